@@ -1,0 +1,22 @@
+"""Weight-only skinny linear layers (NVFP4 / FP8-E4M3 weights, FP16 activations,
+M = 1..8 rows) for GB300, as hand-written sm_103a CUDA kernels behind a C ABI.
+
+The Python surface is a thin ctypes binding with the C names; see
+include/skinny.h for the contract of each call.
+"""
+from ._binding import (  # noqa: F401
+    EXPORTS,
+    LIB_PATH,
+    SK_OK,
+    STATUS,
+    SkinnyError,
+    fp8_gemm,
+    init,
+    last_device_error,
+    lib,
+    lm_head_argmax,
+    nvfp4_gemm,
+    set_pdl,
+    shutdown,
+    status_string,
+)

@@ -1,0 +1,264 @@
+// api.cu -- the C ABI of libskinny (see include/skinny.h): argument checks,
+// workspace management, TMA descriptor encoding and kernel selection.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <atomic>
+#include <mutex>
+
+#include "../../include/skinny.h"
+#include "internal.h"
+#include "kernel.cuh"
+
+namespace {
+
+constexpr int MAX_DEVICES = 64;
+constexpr size_t DEFAULT_WORKSPACE = size_t(64) << 20;
+
+struct DeviceState {
+    unsigned char *ws = nullptr;
+    size_t bytes = 0;
+    int num_sms = 0;
+};
+
+DeviceState g_dev[MAX_DEVICES];
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+int g_pdl = 1;
+std::atomic<int> g_inject_stall{0};
+
+sk_status resolve_encode() {
+    if (g_encode) return SK_OK;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return SK_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return SK_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// 2-D map over a row-major byte matrix viewed as u32 words:
+// dims {row_bytes/4, rows}, row stride row_bytes, box {box_words, 16}.
+bool encode_map(CUtensorMap *m, const void *ptr, uint64_t row_bytes, uint64_t rows, uint32_t box_words) {
+    cuuint64_t dims[2] = {row_bytes / 4, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_words, uint32_t(sk::RG)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(ptr), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Current device's state, or null if sk_init() has not run on it.
+DeviceState *current(int *dev_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return nullptr;
+    if (dev_out) *dev_out = dev;
+    DeviceState *d = &g_dev[dev];
+    return d->ws ? d : nullptr;
+}
+
+// Token count padded to the kernel variant: 1, 2, 4 (SIMT) or 8 (MMA).
+// SK_FORCE_VARIANT=mma makes every M use the MMA variant (for A/B tests).
+int padded_m(int M) {
+    const char *f = std::getenv("SK_FORCE_VARIANT");
+    if (f && std::strcmp(f, "mma") == 0) return 8;
+    if (M <= 1) return 1;
+    if (M == 2) return 2;
+    if (M <= 4) return 4;
+    return 8;
+}
+
+int grid_for(const DeviceState *d, long long units) {
+    long long g = d->num_sms > 0 ? d->num_sms : 1;
+    return int(units < g ? units : g);
+}
+
+enum class Kind { NVFP4, NVFP4_F16, FP8, FP8_F16, LMHEAD };
+
+sk_status zero_outputs(void *y, size_t y_bytes, int32_t *argmax, int M, cudaStream_t s) {
+    if (y && y_bytes && cudaMemsetAsync(y, 0, y_bytes, s) != cudaSuccess) return SK_ERR_CUDA;
+    if (argmax && cudaMemsetAsync(argmax, 0, size_t(M) * 4, s) != cudaSuccess) return SK_ERR_CUDA;
+    return SK_OK;
+}
+
+sk_status run(Kind kind, const void *x, const uint8_t *codes, const void *scales, float gscale, void *y,
+              int32_t *argmax, int M, int N, int K, void *stream) {
+    const bool nv = (kind == Kind::NVFP4 || kind == Kind::NVFP4_F16 || kind == Kind::LMHEAD);
+    const bool f16 = (kind == Kind::NVFP4_F16 || kind == Kind::FP8_F16);
+    const bool am = (kind == Kind::LMHEAD);
+    // ---- argument checks (nothing is launched before these pass)
+    if (M < 1 || M > 8 || N < 0 || K < 0) return SK_ERR_INVALID_ARG;
+    if (am && N < 1) return SK_ERR_INVALID_ARG;
+    if (!x || !codes || !scales) return SK_ERR_INVALID_ARG;
+    if (am ? !argmax : !y) return SK_ERR_INVALID_ARG;
+    if (nv ? (K % 256) : (K % 128)) return SK_ERR_UNSUPPORTED_SHAPE;
+    if (size_t(N) > sk::WS_MAX_ROWGROUPS * sk::RG) return SK_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(x, 16) || !aligned(codes, 16)) return SK_ERR_MISALIGNED;
+    if (nv ? !aligned(scales, 16) : !aligned(scales, 4)) return SK_ERR_MISALIGNED;
+    if (y && !aligned(y, f16 ? 2 : 4)) return SK_ERR_MISALIGNED;
+    if (argmax && !aligned(argmax, 4)) return SK_ERR_MISALIGNED;
+    DeviceState *d = current(nullptr);
+    if (!d) return SK_ERR_NOT_INITIALIZED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (N == 0) return SK_OK;
+    if (K == 0) return zero_outputs(y, size_t(M) * N * (f16 ? 2 : 4), argmax, M, s);
+
+    const int mp = padded_m(M);
+    sk::Params p = {};
+    p.x = reinterpret_cast<const __half *>(x);
+    p.fp8_scales = nv ? nullptr : reinterpret_cast<const float *>(scales);
+    p.gscale = nv ? gscale : 1.0f;
+    p.y = y;
+    p.argmax = argmax;
+    p.ws = d->ws;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.G = (N + sk::RG - 1) / sk::RG;
+    p.C = (K + sk::KC - 1) / sk::KC;
+    p.KB = (K + 127) / 128;
+    p.U = (long long)p.G * p.C;
+    p.stall = g_inject_stall.exchange(0);
+    if (p.C > 1) {
+        const size_t need = size_t(p.U) * sk::unit_partial_bytes(mp);
+        if (sk::WS_PARTIAL_OFFSET + need > d->bytes) return SK_ERR_WORKSPACE;
+    }
+    const int grid = grid_for(d, p.U);
+
+    CUtensorMap tm_codes, tm_scales;
+    if (nv) {
+        if (!encode_map(&tm_codes, codes, uint64_t(K) / 2, uint64_t(N), sk::Traits<sk::NVFP4>::CODE_BOX_X) ||
+            !encode_map(&tm_scales, scales, uint64_t(K) / 16, uint64_t(N), sk::Traits<sk::NVFP4>::SCALE_BOX_X))
+            return SK_ERR_CUDA;
+        if (sk::launch_nvfp4(mp, f16, am, tm_codes, tm_scales, p, grid, s, g_pdl != 0) != cudaSuccess)
+            return SK_ERR_CUDA;
+    } else {
+        if (!encode_map(&tm_codes, codes, uint64_t(K), uint64_t(N), sk::Traits<sk::FP8>::CODE_BOX_X))
+            return SK_ERR_CUDA;
+        if (sk::launch_fp8(mp, f16, tm_codes, p, grid, s, g_pdl != 0) != cudaSuccess) return SK_ERR_CUDA;
+    }
+    return SK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+sk_status sk_init(size_t workspace_bytes) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (resolve_encode() != SK_OK) return SK_ERR_CUDA;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return SK_ERR_CUDA;
+    size_t bytes = workspace_bytes ? workspace_bytes : DEFAULT_WORKSPACE;
+    if (bytes < sk::WS_PARTIAL_OFFSET) bytes = sk::WS_PARTIAL_OFFSET;
+    DeviceState &d = g_dev[dev];
+    if (d.ws) {
+        if (cudaDeviceSynchronize() != cudaSuccess) return SK_ERR_CUDA;
+        cudaFree(d.ws);
+        d.ws = nullptr;
+        d.bytes = 0;
+    }
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SK_ERR_CUDA;
+    void *p = nullptr;
+    if (cudaMalloc(&p, bytes) != cudaSuccess) return SK_ERR_CUDA;
+    if (cudaMemset(p, 0, bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+        cudaFree(p);
+        return SK_ERR_CUDA;
+    }
+    d.ws = static_cast<unsigned char *>(p);
+    d.bytes = bytes;
+    d.num_sms = sms;
+    return SK_OK;
+}
+
+sk_status sk_shutdown(void) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    int prev = 0;
+    cudaGetDevice(&prev);
+    sk_status st = SK_OK;
+    for (int i = 0; i < MAX_DEVICES; ++i) {
+        if (!g_dev[i].ws) continue;
+        if (cudaSetDevice(i) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) st = SK_ERR_CUDA;
+        cudaFree(g_dev[i].ws);
+        g_dev[i] = DeviceState{};
+    }
+    cudaSetDevice(prev);
+    return st;
+}
+
+sk_status nvfp4_gemm(const void *x, const uint8_t *W_codes, const uint8_t *W_scales, float W_gscale, float *y,
+                     int M, int N, int K, void *stream) {
+    return run(Kind::NVFP4, x, W_codes, W_scales, W_gscale, y, nullptr, M, N, K, stream);
+}
+
+sk_status nvfp4_gemm_f16out(const void *x, const uint8_t *W_codes, const uint8_t *W_scales, float W_gscale,
+                            void *y, int M, int N, int K, void *stream) {
+    return run(Kind::NVFP4_F16, x, W_codes, W_scales, W_gscale, y, nullptr, M, N, K, stream);
+}
+
+sk_status fp8_gemm(const void *x, const uint8_t *W_codes, const float *W_scales, float *y, int M, int N, int K,
+                   void *stream) {
+    return run(Kind::FP8, x, W_codes, W_scales, 1.0f, y, nullptr, M, N, K, stream);
+}
+
+sk_status fp8_gemm_f16out(const void *x, const uint8_t *W_codes, const float *W_scales, void *y, int M, int N,
+                          int K, void *stream) {
+    return run(Kind::FP8_F16, x, W_codes, W_scales, 1.0f, y, nullptr, M, N, K, stream);
+}
+
+sk_status lm_head_argmax(const void *x, const uint8_t *W_codes, const uint8_t *W_scales, float W_gscale,
+                         float *logits, int32_t *argmax, int M, int N, int K, void *stream) {
+    return run(Kind::LMHEAD, x, W_codes, W_scales, W_gscale, logits, argmax, M, N, K, stream);
+}
+
+const char *sk_status_string(sk_status status) {
+    switch (status) {
+        case SK_OK: return "SK_OK";
+        case SK_ERR_INVALID_ARG: return "SK_ERR_INVALID_ARG: invalid argument";
+        case SK_ERR_UNSUPPORTED_SHAPE: return "SK_ERR_UNSUPPORTED_SHAPE: unsupported shape";
+        case SK_ERR_MISALIGNED: return "SK_ERR_MISALIGNED: misaligned pointer";
+        case SK_ERR_NOT_INITIALIZED: return "SK_ERR_NOT_INITIALIZED: sk_init() not called on this device";
+        case SK_ERR_CUDA: return "SK_ERR_CUDA: CUDA error";
+        case SK_ERR_TIMEOUT: return "SK_ERR_TIMEOUT: a bounded in-kernel wait timed out";
+        case SK_ERR_WORKSPACE: return "SK_ERR_WORKSPACE: workspace too small";
+    }
+    return "unknown sk_status";
+}
+
+sk_status sk_last_device_error(void *stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SK_ERR_CUDA;
+    DeviceState *d = current(nullptr);
+    if (!d) return SK_ERR_NOT_INITIALIZED;
+    unsigned int err = 0;
+    unsigned char *word = d->ws + offsetof(sk::Ctrl, err);
+    if (cudaMemcpy(&err, word, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess) return SK_ERR_CUDA;
+    if (err) {
+        if (cudaMemset(word, 0, sizeof(err)) != cudaSuccess) return SK_ERR_CUDA;
+        return SK_ERR_TIMEOUT;
+    }
+    return SK_OK;
+}
+
+int sk_set_pdl(int enable) {
+    int prev = g_pdl;
+    g_pdl = enable ? 1 : 0;
+    return prev;
+}
+
+void sk_inject_wait_timeout(int enable) { g_inject_stall.store(enable ? 1 : 0); }
+
+int sk_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,21 @@
+// internal.h -- declarations shared by the host translation units of libskinny.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace sk {
+
+struct Params;
+
+// Launch one kernel of the given format.  mp: padded token count
+// (1, 2, 4 = SIMT path; 8 = MMA path).
+cudaError_t launch_nvfp4(int mp, bool f16out, bool argmax, const CUtensorMap &tm_codes,
+                         const CUtensorMap &tm_scales, const Params &p, int grid,
+                         cudaStream_t stream, bool pdl);
+cudaError_t launch_fp8(int mp, bool f16out, const CUtensorMap &tm_codes, const Params &p, int grid,
+                       cudaStream_t stream, bool pdl);
+
+// Bytes of workspace-resident partial sums one unit writes (16 rows x mp tokens).
+inline size_t unit_partial_bytes(int mp) { return size_t(16) * mp * 4; }
+
+}  // namespace sk

@@ -1,0 +1,12 @@
+// k_fp8.cu -- instantiations of the FP8 kernel variants.
+#include "launch.cuh"
+
+namespace sk {
+
+cudaError_t launch_fp8(int mp, bool f16out, const CUtensorMap &tm_codes, const Params &p, int grid,
+                       cudaStream_t stream, bool pdl) {
+    if (f16out) return launch_by_m<FP8, true, false>(mp, tm_codes, tm_codes, p, grid, stream, pdl);
+    return launch_by_m<FP8, false, false>(mp, tm_codes, tm_codes, p, grid, stream, pdl);
+}
+
+}  // namespace sk

@@ -1,0 +1,14 @@
+// k_nvfp4.cu -- instantiations of the NVFP4 kernel variants.
+#include "launch.cuh"
+
+namespace sk {
+
+cudaError_t launch_nvfp4(int mp, bool f16out, bool argmax, const CUtensorMap &tm_codes,
+                         const CUtensorMap &tm_scales, const Params &p, int grid,
+                         cudaStream_t stream, bool pdl) {
+    if (argmax) return launch_by_m<NVFP4, false, true>(mp, tm_codes, tm_scales, p, grid, stream, pdl);
+    if (f16out) return launch_by_m<NVFP4, true, false>(mp, tm_codes, tm_scales, p, grid, stream, pdl);
+    return launch_by_m<NVFP4, false, false>(mp, tm_codes, tm_scales, p, grid, stream, pdl);
+}
+
+}  // namespace sk

@@ -1,0 +1,560 @@
+// kernel.cuh -- the skinny weight-only linear kernel for sm_103a.
+//
+// One persistent CTA per SM streams compressed weight tiles HBM -> shared
+// memory with 2-D TMA into an mbarrier ring, and two consumer groups of four
+// warps decode them in registers and multiply-accumulate in FP32:
+//
+//   * M <= 4 ("SIMT" path): E2M1 / E4M3 pairs -> f16x2 with cvt.rn.f16x2.*,
+//     exact FP16 products accumulated in FP32 with the mixed-precision FMA,
+//     the 16-element (NVFP4) or 128x128 (FP8) block scale applied once per
+//     block sum.
+//   * M = 5..8 ("MMA" path, the 8-row speculative-verify round): swap-AB
+//     mma.sync.m16n8k16 with the 16 weight rows as the 16-wide operand and the
+//     (zero-padded) 8 tokens as the 8-wide one.  For NVFP4 each decoded pair
+//     is multiplied by its E4M3 block scale in FP16 first, which is exact
+//     (E2M1 has 2 and E4M3 4 significant bits, and their product stays in the
+//     FP16 normal range), so the MMA sees exact weights and accumulates in
+//     FP32.  For FP8 the per-block scale multiplies the FP32 accumulators.
+//
+// This is the decode-time linear layer of the pages' system, where weights are
+// read compressed from HBM and each small piece becomes FP16 register
+// operands (page "NVFP4 在 Volta 上！", section "我实际构建了什么"), and the
+// 8-row tensor-core tile carries the k=7 verify round (same page, the
+// paragraph after the kernel table).  The Volta design itself (HMMA.884, the
+// SIMT kernel) is not reproduced: the ring, TMA and the block-scale folding are
+// this library's.
+//
+// Work decomposition ("units").  A unit is RG = 16 weight rows x KC = 1024 k.
+// Units are numbered chunk-major, u = c * G + g (G row groups, C k-chunks),
+// and CTA b takes the contiguous range [b*U/P, (b+1)*U/P), so every CTA
+// streams the same number of bytes (+-1 unit) whatever the shape.  Each unit
+// yields a 16 x MP partial sum; when C > 1 it goes to the workspace and the
+// CTA that delivers the last partial of a row group (an atomic counter per row
+// group) sums the C partials in ascending chunk order and writes y.  The sum
+// order is therefore fixed: results are bitwise reproducible.
+#pragma once
+#include <cuda.h>
+#include <cstdint>
+#include <cuda_fp16.h>
+#include "ptx.cuh"
+
+namespace sk {
+
+enum Fmt : int { NVFP4 = 0, FP8 = 1 };
+
+constexpr int RG = 16;            // weight rows per unit
+constexpr int KC = 1024;          // k per unit
+constexpr int NGROUPS = 2;        // consumer groups per CTA
+constexpr int GROUP_THREADS = 128;
+constexpr int CTA_THREADS = NGROUPS * GROUP_THREADS + 32;   // + one producer warp
+constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;            // bounded waits: ~1 s
+
+// Workspace layout (bytes): control block, row-group counters, partial sums.
+constexpr size_t WS_CTRL_BYTES = 4096;
+constexpr size_t WS_MAX_ROWGROUPS = size_t(1) << 18;
+constexpr size_t WS_PARTIAL_OFFSET = WS_CTRL_BYTES + WS_MAX_ROWGROUPS * 4;
+
+struct Ctrl {
+    unsigned long long argmax_key[8];   // per token: (ordered logit << 32) | ~n
+    unsigned int done;                  // CTAs finished (argmax epilogue)
+    unsigned int err;                   // device error word (bit 0: a wait timed out)
+};
+
+enum : unsigned int { ERR_TIMEOUT = 1u };
+
+template <int FMT> struct Traits;
+template <> struct Traits<NVFP4> {
+    static constexpr int ROW_BYTES = KC / 2;           // codes of one row in a unit
+    static constexpr int CODE_TILE = RG * ROW_BYTES;   // 8192
+    static constexpr int SCALE_ROW = KC / 16;          // 64 E4M3 scales per row
+    static constexpr int SCALE_TILE = RG * SCALE_ROW;  // 1024
+    static constexpr int STAGE_BYTES = CODE_TILE + SCALE_TILE;
+    static constexpr int STAGES = 8;
+    static constexpr int CODE_BOX_X = ROW_BYTES / 4;   // tensor map element = u32
+    static constexpr int SCALE_BOX_X = SCALE_ROW / 4;
+};
+template <> struct Traits<FP8> {
+    static constexpr int ROW_BYTES = KC;
+    static constexpr int CODE_TILE = RG * ROW_BYTES;   // 16384
+    static constexpr int SCALE_TILE = 0;
+    static constexpr int STAGE_BYTES = CODE_TILE;
+    static constexpr int STAGES = 6;
+    static constexpr int CODE_BOX_X = ROW_BYTES / 4;
+    static constexpr int SCALE_BOX_X = 0;
+};
+
+struct Params {
+    const __half *x;            // [M][K]
+    const float *fp8_scales;    // FP8: [ceil(N/128)][KB]
+    float gscale;               // NVFP4 tensor scale (1 for FP8)
+    void *y;                    // [M][N] f32 or f16; may be null with ARGMAX
+    int32_t *argmax;            // [M] (ARGMAX only)
+    unsigned char *ws;          // workspace base
+    int M, N, K;
+    int G, C, KB;               // row groups, k-chunks, FP8 scale row stride
+    long long U;                // units = G * C
+    int stall;                  // failure injection: the producer issues no copies
+};
+
+template <int FMT, int MP>
+__host__ __device__ constexpr int red_floats() { return MP == 8 ? 4 * 128 : RG * MP; }
+
+template <int FMT, int MP>
+__host__ __device__ constexpr size_t smem_bytes() {
+    return 1024 + size_t(Traits<FMT>::STAGES) * Traits<FMT>::STAGE_BYTES +
+           16 * Traits<FMT>::STAGES + NGROUPS * red_floats<FMT, MP>() * 4 + 64 +
+           NGROUPS * GROUP_THREADS * 8;
+}
+
+// Bounded mbarrier wait.  Gives up when the CTA's abort flag is set or after
+// WAIT_LIMIT_NS; on a timeout it raises the abort flag and the device error
+// word.  Returns false when it gave up.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort,
+                                             unsigned int *err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+                *abort = 1;
+                atomicOr(err, ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// Order-preserving map of an FP32 value to u32 (larger value -> larger key).
+__device__ __forceinline__ unsigned int ordered_bits(float v) {
+    unsigned int u = __float_as_uint(v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Warp reduction of NV values per lane.  Afterwards lane l holds the full sum
+// of value index reduce_index<NV>(l) in v[0].
+template <int NV>
+__device__ __forceinline__ void warp_reduce_split(float (&v)[NV], int lane) {
+    int n = NV;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        if (n > 1) {
+            const int h = n / 2;
+            const bool upper = (lane & o) != 0;
+#pragma unroll
+            for (int e = 0; e < NV / 2; ++e) {
+                if (e < h) {
+                    float send = upper ? v[e] : v[e + h];
+                    float keep = upper ? v[e + h] : v[e];
+                    v[e] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                }
+            }
+            n = h;
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+        }
+    }
+}
+
+template <int NV>
+__device__ __forceinline__ int reduce_index(int lane) {
+    int idx = 0, n = NV;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        if (n > 1) {
+            const int h = n / 2;
+            if (lane & o) idx += h;
+            n = h;
+        }
+    }
+    return idx;
+}
+
+// ----------------------------------------------------------------------------
+// Activation registers for one k-chunk.
+//   MMA (MP == 8): lane (j = lane/4, q = lane%4) of warp w holds, for each of
+//     the 32 mma k-steps of its k slice, the B fragment of token j.
+//   SIMT: lane l holds 32 activations (16 f16x2 words) per token.
+// Tokens >= M and k >= K read as zero.
+template <int FMT, int MP>
+struct XRegs {
+    static constexpr int PIECES = (MP == 8) ? (FMT == NVFP4 ? 2 : 4) : 1;
+    static constexpr int WORDS = (MP == 8) ? (FMT == NVFP4 ? 16 : 8) : 16;
+    static constexpr int TOK = (MP == 8) ? 1 : MP;
+    uint32_t w[TOK][PIECES][WORDS];
+};
+
+template <int FMT, int MP>
+__device__ __forceinline__ void load_x(XRegs<FMT, MP> &xr, const Params &p, int c, int warp_in_group,
+                                       int lane) {
+    const int kbase = c * KC;
+    if constexpr (MP == 8) {
+        const int j = lane >> 2, q = lane & 3;
+#pragma unroll
+        for (int t = 0; t < XRegs<FMT, MP>::PIECES; ++t) {
+            const int k0 = (FMT == NVFP4) ? kbase + 256 * warp_in_group + 128 * t + 32 * q
+                                          : kbase + 256 * warp_in_group + 64 * t + 16 * q;
+#pragma unroll
+            for (int v = 0; v < XRegs<FMT, MP>::WORDS / 4; ++v) {
+                const int k = k0 + 8 * v;
+                uint4 val = make_uint4(0, 0, 0, 0);
+                if (j < p.M && k < p.K) val = ld_global_v4(p.x + size_t(j) * p.K + k);
+                xr.w[0][t][4 * v + 0] = val.x;
+                xr.w[0][t][4 * v + 1] = val.y;
+                xr.w[0][t][4 * v + 2] = val.z;
+                xr.w[0][t][4 * v + 3] = val.w;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int m = 0; m < MP; ++m) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                // NVFP4: k = 32*lane + 8v;  FP8: pieces [16*lane, +16) and [512 + 16*lane, +16)
+                const int k = (FMT == NVFP4) ? kbase + 32 * lane + 8 * v
+                                             : kbase + (v >> 1) * 512 + 16 * lane + 8 * (v & 1);
+                uint4 val = make_uint4(0, 0, 0, 0);
+                if (m < p.M && k < p.K) val = ld_global_v4(p.x + size_t(m) * p.K + k);
+                xr.w[m][0][4 * v + 0] = val.x;
+                xr.w[m][0][4 * v + 1] = val.y;
+                xr.w[m][0][4 * v + 2] = val.z;
+                xr.w[m][0][4 * v + 3] = val.w;
+            }
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------
+// MMA path, one unit, one warp: D (16 rows x 8 tokens) of this warp's k slice.
+template <int FMT>
+__device__ __forceinline__ void unit_mma(float (&d)[4], const XRegs<FMT, 8> &xr, uint32_t stage,
+                                         const Params &p, int g, int c, int w, int lane) {
+    const int r = lane >> 2, q = lane & 3;
+    if constexpr (FMT == NVFP4) {
+        const uint32_t codes = stage, scales = stage + Traits<NVFP4>::CODE_TILE;
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const uint32_t off = 128 * w + 64 * t + 16 * q;
+            const uint4 A = ld_shared_v4(codes + r * 512 + off);
+            const uint4 B = ld_shared_v4(codes + (r + 8) * 512 + off);
+            const uint32_t soff = 16 * w + 8 * t + 2 * q;
+            const uint32_t sa = e4m3x2_to_f16x2<0>(ld_shared_u16(scales + r * 64 + soff));
+            const uint32_t sb = e4m3x2_to_f16x2<0>(ld_shared_u16(scales + (r + 8) * 64 + soff));
+            const uint32_t sa0 = bcast_lo(sa), sa1 = bcast_hi(sa);
+            const uint32_t sb0 = bcast_lo(sb), sb1 = bcast_hi(sb);
+            const uint32_t Aw[4] = {A.x, A.y, A.z, A.w};
+            const uint32_t Bw[4] = {B.x, B.y, B.z, B.w};
+#pragma unroll
+            for (int ii = 0; ii < 8; ++ii) {
+                const uint32_t wa = Aw[ii >> 1], wb = Bw[ii >> 1];
+                const uint32_t s_a = ii < 4 ? sa0 : sa1;
+                const uint32_t s_b = ii < 4 ? sb0 : sb1;
+                uint32_t a0, a1, a2, a3;
+                if (ii & 1) {
+                    a0 = hmul2(e2m1x2_to_f16x2<2>(wa), s_a);
+                    a1 = hmul2(e2m1x2_to_f16x2<2>(wb), s_b);
+                    a2 = hmul2(e2m1x2_to_f16x2<3>(wa), s_a);
+                    a3 = hmul2(e2m1x2_to_f16x2<3>(wb), s_b);
+                } else {
+                    a0 = hmul2(e2m1x2_to_f16x2<0>(wa), s_a);
+                    a1 = hmul2(e2m1x2_to_f16x2<0>(wb), s_b);
+                    a2 = hmul2(e2m1x2_to_f16x2<1>(wa), s_a);
+                    a3 = hmul2(e2m1x2_to_f16x2<1>(wb), s_b);
+                }
+                mma_16816(acc[ii & 1], a0, a1, a2, a3, xr.w[0][t][2 * ii], xr.w[0][t][2 * ii + 1]);
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) d[e] = acc[0][e] + acc[1][e];
+    } else {
+        const uint32_t codes = stage;
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const uint32_t off = 256 * w + 64 * t + 16 * q;
+            const uint4 A = ld_shared_v4(codes + r * 1024 + off);
+            const uint4 B = ld_shared_v4(codes + (r + 8) * 1024 + off);
+            const uint32_t Aw[4] = {A.x, A.y, A.z, A.w};
+            const uint32_t Bw[4] = {B.x, B.y, B.z, B.w};
+#pragma unroll
+            for (int ii = 0; ii < 4; ++ii) {
+                mma_16816(acc[t >> 1], e4m3x2_to_f16x2<0>(Aw[ii]), e4m3x2_to_f16x2<0>(Bw[ii]),
+                          e4m3x2_to_f16x2<1>(Aw[ii]), e4m3x2_to_f16x2<1>(Bw[ii]),
+                          xr.w[0][t][2 * ii], xr.w[0][t][2 * ii + 1]);
+            }
+        }
+        const int rb = g >> 3;                  // 128-row block of this row group
+        const int kb0 = c * (KC / 128) + 2 * w; // 128-k blocks of this warp's slice
+        const float *srow = p.fp8_scales + size_t(rb) * p.KB;
+        const float s0 = kb0 < p.KB ? __ldg(srow + kb0) : 0.f;
+        const float s1 = kb0 + 1 < p.KB ? __ldg(srow + kb0 + 1) : 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) d[e] = acc[0][e] * s0 + acc[1][e] * s1;
+    }
+}
+
+// SIMT path, one unit, one warp: out[i][m] for rows 4w+i of the unit.
+template <int FMT, int MP>
+__device__ __forceinline__ void unit_simt(float (&out)[4 * MP], const XRegs<FMT, MP> &xr,
+                                          uint32_t stage, const Params &p, int g, int c, int w,
+                                          int lane) {
+    if constexpr (FMT == NVFP4) {
+        const uint32_t codes = stage, scales = stage + Traits<NVFP4>::CODE_TILE;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int row = 4 * w + i;
+            const uint4 A = ld_shared_v4(codes + row * 512 + 16 * lane);
+            const float2 sf = f16x2_to_f32x2(e4m3x2_to_f16x2<0>(ld_shared_u16(scales + row * 64 + 2 * lane)));
+            const uint32_t Aw[4] = {A.x, A.y, A.z, A.w};
+            float b0[MP], b1[MP];
+#pragma unroll
+            for (int m = 0; m < MP; ++m) { b0[m] = 0.f; b1[m] = 0.f; }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                uint32_t wv;
+                switch (j & 3) {
+                    case 0: wv = e2m1x2_to_f16x2<0>(Aw[j >> 2]); break;
+                    case 1: wv = e2m1x2_to_f16x2<1>(Aw[j >> 2]); break;
+                    case 2: wv = e2m1x2_to_f16x2<2>(Aw[j >> 2]); break;
+                    default: wv = e2m1x2_to_f16x2<3>(Aw[j >> 2]); break;
+                }
+#pragma unroll
+                for (int m = 0; m < MP; ++m) {
+                    if (j < 8) b0[m] = fma2_f16_f32(wv, xr.w[m][0][j], b0[m]);
+                    else       b1[m] = fma2_f16_f32(wv, xr.w[m][0][j], b1[m]);
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < MP; ++m) out[i * MP + m] = b0[m] * sf.x + b1[m] * sf.y;
+        }
+    } else {
+        const uint32_t codes = stage;
+        const int rb = g >> 3;
+        const int kb0 = c * (KC / 128) + (lane >> 3);
+        const float *srow = p.fp8_scales + size_t(rb) * p.KB;
+        const float s0 = kb0 < p.KB ? __ldg(srow + kb0) : 0.f;
+        const float s1 = kb0 + 4 < p.KB ? __ldg(srow + kb0 + 4) : 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int row = 4 * w + i;
+            const uint4 A0 = ld_shared_v4(codes + row * 1024 + 16 * lane);
+            const uint4 A1 = ld_shared_v4(codes + row * 1024 + 512 + 16 * lane);
+            const uint32_t Aw[8] = {A0.x, A0.y, A0.z, A0.w, A1.x, A1.y, A1.z, A1.w};
+            float p0[MP], p1[MP];
+#pragma unroll
+            for (int m = 0; m < MP; ++m) { p0[m] = 0.f; p1[m] = 0.f; }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const uint32_t wv = (j & 1) ? e4m3x2_to_f16x2<1>(Aw[j >> 1]) : e4m3x2_to_f16x2<0>(Aw[j >> 1]);
+#pragma unroll
+                for (int m = 0; m < MP; ++m) {
+                    if (j < 8) p0[m] = fma2_f16_f32(wv, xr.w[m][0][j], p0[m]);
+                    else       p1[m] = fma2_f16_f32(wv, xr.w[m][0][j], p1[m]);
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < MP; ++m) out[i * MP + m] = p0[m] * s0 + p1[m] * s1;
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------
+template <int FMT, int MP, bool F16OUT, bool ARGMAX>
+__global__ void __launch_bounds__(CTA_THREADS, 2)
+skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
+              const Params p) {
+    using T = Traits<FMT>;
+    constexpr int RED = red_floats<FMT, MP>();
+    constexpr int NOUT = RG * MP;                 // outputs per unit
+
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char *sb = smem_raw + (base - raw);
+    const uint32_t bar_full = base + T::STAGES * T::STAGE_BYTES;
+    const uint32_t bar_empty = bar_full + 8 * T::STAGES;
+    float *red = reinterpret_cast<float *>(sb + T::STAGES * T::STAGE_BYTES + 16 * T::STAGES);
+    volatile int *flags = reinterpret_cast<volatile int *>(red + NGROUPS * RED);   // [0] abort, [1+q] last
+    unsigned long long *keys = reinterpret_cast<unsigned long long *>(
+        sb + T::STAGES * T::STAGE_BYTES + 16 * T::STAGES + NGROUPS * RED * 4 + 64);
+
+    Ctrl *ctrl = reinterpret_cast<Ctrl *>(p.ws);
+    unsigned int *counters = reinterpret_cast<unsigned int *>(p.ws + WS_CTRL_BYTES);
+    float *partials = reinterpret_cast<float *>(p.ws + WS_PARTIAL_OFFSET);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long u_lo = (long long)blockIdx.x * p.U / gridDim.x;
+    const long long u_hi = (long long)(blockIdx.x + 1) * p.U / gridDim.x;
+    const int n_units = int(u_hi - u_lo);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < T::STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 4);
+        }
+        flags[0] = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    // Let the next kernel on the stream start streaming its own weights now;
+    // it touches x / y / the workspace only after this grid has completed.
+    pdl_launch_dependents();
+
+    if (warp == NGROUPS * 4) {
+        // ------------------------------------------------------ producer ---
+        if (lane == 0) {
+            const uint64_t pol = l2_evict_first_policy();
+            int issued = 0;
+            for (int i = 0; i < (p.stall ? 0 : n_units); ++i) {
+                const int s = i % T::STAGES;
+                if (i >= T::STAGES &&
+                    !wait_bounded(bar_empty + 8 * s, ((i / T::STAGES) & 1) ^ 1, flags, &ctrl->err))
+                    break;
+                const long long u = u_lo + i;
+                const int c = int(u / p.G), g = int(u % p.G);
+                const uint32_t dst = base + s * T::STAGE_BYTES;
+                mbar_arrive_expect_tx(bar_full + 8 * s, T::STAGE_BYTES);
+                tma_load_2d(dst, &tm_codes, bar_full + 8 * s, c * T::CODE_BOX_X, g * RG, pol);
+                if constexpr (FMT == NVFP4)
+                    tma_load_2d(dst + T::CODE_TILE, &tm_scales, bar_full + 8 * s, c * T::SCALE_BOX_X,
+                                g * RG, pol);
+                issued = i + 1;
+            }
+            if (flags[0]) {
+                // Aborted: let the copies still in flight land before exiting.
+                for (int i = issued - T::STAGES < 0 ? 0 : issued - T::STAGES; i < issued; ++i) {
+                    const int s = i % T::STAGES;
+                    const uint64_t t0 = globaltimer_ns();
+                    while (!mbar_try_wait(bar_full + 8 * s, (i / T::STAGES) & 1) &&
+                           globaltimer_ns() - t0 < WAIT_LIMIT_NS) {
+                    }
+                }
+            }
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------ consumers ---
+    const int q = warp >> 2, w = warp & 3;
+    const int t = threadIdx.x - q * GROUP_THREADS;     // 0..127 within the group
+    const uint32_t bar_id = 1 + q;
+    float *gred = red + q * RED;
+    unsigned long long best = 0;                       // ARGMAX: best key of token t % MP
+
+    pdl_wait_primary();
+
+    XRegs<FMT, MP> xr;
+    int cur_c = -1;
+    for (int i = q; i < n_units; i += NGROUPS) {
+        const long long u = u_lo + i;
+        const int c = int(u / p.G), g = int(u % p.G);
+        if (c != cur_c) {
+            load_x<FMT, MP>(xr, p, c, w, lane);
+            cur_c = c;
+        }
+        const int s = i % T::STAGES;
+        wait_bounded(bar_full + 8 * s, (i / T::STAGES) & 1, flags, &ctrl->err);
+        const uint32_t stage = base + s * T::STAGE_BYTES;
+
+        if constexpr (MP == 8) {
+            float d[4];
+            unit_mma<FMT>(d, xr, stage, p, g, c, w, lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+            const int r = lane >> 2, qq = lane & 3;
+            *reinterpret_cast<float2 *>(gred + w * 128 + r * 8 + 2 * qq) = make_float2(d[0], d[1]);
+            *reinterpret_cast<float2 *>(gred + w * 128 + (r + 8) * 8 + 2 * qq) = make_float2(d[2], d[3]);
+        } else {
+            float out[4 * MP];
+            unit_simt<FMT, MP>(out, xr, stage, p, g, c, w, lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+            warp_reduce_split<4 * MP>(out, lane);
+            constexpr int NV = 4 * MP;
+            // lanes holding a distinct value: the lowest lane of each run
+            const int idx = reduce_index<NV>(lane);
+            if ((lane & ((32 / NV) - 1)) == 0) gred[(4 * w) * MP + idx] = out[0];
+        }
+        named_bar_sync(bar_id, GROUP_THREADS);
+
+        // value of output t of this unit (row t / MP, token t % MP)
+        float v = 0.f;
+        if (t < NOUT) {
+            if constexpr (MP == 8) v = gred[t] + gred[128 + t] + gred[256 + t] + gred[384 + t];
+            else v = gred[t];
+        }
+        bool final_here = (p.C == 1);
+        if (!final_here) {
+            if (t < NOUT) partials[((size_t)g * p.C + c) * NOUT + t] = v;
+            __threadfence();
+            named_bar_sync(bar_id, GROUP_THREADS);
+            if (t == 0) {
+                const unsigned int old = atomicAdd(counters + g, 1u);
+                flags[1 + q] = (old == unsigned(p.C - 1));
+            }
+            named_bar_sync(bar_id, GROUP_THREADS);
+            final_here = flags[1 + q] != 0;
+            if (final_here) {
+                __threadfence();
+                if (t < NOUT) {
+                    const float *src = partials + (size_t)g * p.C * NOUT + t;
+                    float acc = ld_cg_f32(src);
+                    for (int cc = 1; cc < p.C; ++cc) acc += ld_cg_f32(src + (size_t)cc * NOUT);
+                    v = acc;
+                }
+                if (t == 0) counters[g] = 0u;
+            }
+        } else {
+            named_bar_sync(bar_id, GROUP_THREADS);   // gred is reused by the next unit
+        }
+        if (final_here && t < NOUT) {
+            const int row = t / MP, m = t % MP;
+            const int n = g * RG + row;
+            const float val = (FMT == NVFP4) ? v * p.gscale : v;
+            if (n < p.N && m < p.M) {
+                if (p.y) {
+                    if constexpr (F16OUT) reinterpret_cast<__half *>(p.y)[size_t(m) * p.N + n] = __float2half_rn(val);
+                    else reinterpret_cast<float *>(p.y)[size_t(m) * p.N + n] = val;
+                }
+                if constexpr (ARGMAX) {
+                    const unsigned long long key =
+                        (static_cast<unsigned long long>(ordered_bits(val)) << 32) | static_cast<unsigned int>(~n);
+                    best = key > best ? key : best;
+                }
+            }
+        }
+    }
+
+    if constexpr (ARGMAX) {
+        // Per-CTA best per token -> one 64-bit atomicMax per token; the last CTA
+        // to finish turns the keys into indices and resets them.
+        keys[q * GROUP_THREADS + t] = best;
+        named_bar_sync(15, NGROUPS * GROUP_THREADS);
+        if (q == 0 && t < MP) {
+            unsigned long long k = 0;
+            for (int e = t; e < NGROUPS * GROUP_THREADS; e += MP) {
+                const int te = e % GROUP_THREADS;
+                if (te < NOUT) k = keys[e] > k ? keys[e] : k;
+            }
+            if (k != 0 && t < p.M) atomicMax(&ctrl->argmax_key[t], k);
+            __threadfence();
+        }
+        named_bar_sync(15, NGROUPS * GROUP_THREADS);
+        if (q == 0 && t == 0) {
+            const unsigned int old = atomicAdd(&ctrl->done, 1u);
+            if (old == gridDim.x - 1) {
+                __threadfence();
+                for (int m = 0; m < p.M; ++m) {
+                    const unsigned long long k = ld_cg_u64(&ctrl->argmax_key[m]);
+                    p.argmax[m] = static_cast<int32_t>(~static_cast<unsigned int>(k & 0xffffffffull));
+                    ctrl->argmax_key[m] = 0ull;
+                }
+                ctrl->done = 0u;
+            }
+        }
+    }
+}
+
+}  // namespace sk

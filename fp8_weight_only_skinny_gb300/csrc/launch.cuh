@@ -1,0 +1,48 @@
+// launch.cuh -- host-side launch of the skinny kernel variants.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include "kernel.cuh"
+#include "internal.h"
+
+namespace sk {
+
+template <int FMT, int MP, bool F16OUT, bool ARGMAX>
+cudaError_t launch_variant(const CUtensorMap &tm_codes, const CUtensorMap &tm_scales, const Params &p,
+                           int grid, cudaStream_t stream, bool pdl) {
+    auto kfn = skinny_kernel<FMT, MP, F16OUT, ARGMAX>;
+    constexpr size_t smem = smem_bytes<FMT, MP>();
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !attr_done[dev]) {
+        e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(CTA_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kfn, tm_codes, tm_scales, p);
+}
+
+template <int FMT, bool F16OUT, bool ARGMAX>
+cudaError_t launch_by_m(int mp, const CUtensorMap &tm_codes, const CUtensorMap &tm_scales,
+                        const Params &p, int grid, cudaStream_t stream, bool pdl) {
+    switch (mp) {
+        case 1: return launch_variant<FMT, 1, F16OUT, ARGMAX>(tm_codes, tm_scales, p, grid, stream, pdl);
+        case 2: return launch_variant<FMT, 2, F16OUT, ARGMAX>(tm_codes, tm_scales, p, grid, stream, pdl);
+        case 4: return launch_variant<FMT, 4, F16OUT, ARGMAX>(tm_codes, tm_scales, p, grid, stream, pdl);
+        default: return launch_variant<FMT, 8, F16OUT, ARGMAX>(tm_codes, tm_scales, p, grid, stream, pdl);
+    }
+}
+
+}  // namespace sk

@@ -1,0 +1,179 @@
+/*
+ * skinny.h -- C ABI of libskinny, the weight-only "skinny" linear layer for
+ * GB300 (sm_103a):
+ *
+ *     y[m][n] = sum_k x[m][k] * w[n][k]      m < M <= 8,  n < N,  k < K
+ *
+ * with FP16 activations x and weights w that stay compressed in device memory
+ * and are decoded in registers inside the kernel, with no "dequantize the
+ * model first" pass.  This is the decode-time linear layer of the pages'
+ * system: weight bandwidth dominates single-request decode, the weights are
+ * read compressed from HBM and each small piece is turned into FP16 register
+ * operands (page "NVFP4 在 Volta 上！", section "我实际构建了什么"); M = 1 is one
+ * decode token, M = 8 the k=7 speculative-verify round packed as 8 rows (same
+ * page, kernel table "路径 有效带宽 测量读取上限" and the paragraph after it).
+ *
+ * Weight formats (the pages name NVFP4 and FP8-E4M3 regions of the checkpoint,
+ * page "NVFP4 在 Volta 上！", section on v1.1; the layouts are this library's):
+ *
+ *   NVFP4  W_codes  u8 [N][K/2]  two E2M1 codes per byte, LOW nibble = even k
+ *          W_scales u8 [N][K/16] one E4M3 scale per 16 consecutive k of a row
+ *          W_gscale f32          one tensor scale
+ *          w[n][k] = E2M1(code) * E4M3(W_scales[n][k/16]) * W_gscale
+ *   FP8    W_codes  u8 [N][K]    E4M3 codes
+ *          W_scales f32 [ceil(N/128)][ceil(K/128)] one scale per 128x128 block
+ *          w[n][k] = E4M3(code) * W_scales[n/128][k/128]
+ *
+ *   E2M1 is the OCP MX FP4 element type; E4M3 is the OCP OFP8 "E4M3" type
+ *   (no infinities, S.1111.111 = NaN).
+ *
+ * Common rules for every entry point
+ *   - x is FP16, row-major [M][K]; y is row-major [M][N].  All pointers are
+ *     device pointers owned by the caller; the library keeps none of them.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream), do no host synchronisation and allocate nothing: the
+ *     split-K partial sums and the argmax partials live in the workspace that
+ *     sk_init() allocated for the current device.
+ *   - Arguments are checked before anything is launched; a rejected call
+ *     launches nothing and returns the status code.  Launch failures return
+ *     SK_ERR_CUDA.
+ *   - Determinism: a given (shape, device) always sums in the same order, so
+ *     repeated calls are bitwise identical.  Split-K partials are combined in a
+ *     fixed order, never with floating-point atomics.
+ *   - Accuracy contract (FP32 accumulation of exact FP16 products):
+ *       |y - y_exact| <= 1e-3 * sum_k |x[m][k] * w[n][k]| + 1e-6
+ *     plus one FP16 ulp of the result for the *_f16out variants.
+ *   - One stream at a time per workspace: calls whose kernels overlap in time
+ *     on different streams of the same device race on the workspace.
+ *     Consecutive calls on one stream may overlap through programmatic
+ *     dependent launch: a kernel may start streaming its own weights while the
+ *     previous kernel of this library finishes, but touches x, y and the
+ *     workspace only after that kernel has completed.  So weights must not be
+ *     written by the kernel immediately preceding the call on the same stream
+ *     if that kernel is one of this library's (none of them writes weights).
+ *   - Kernels bound every wait they spin on (about one second).  When a wait
+ *     runs out the kernel records SK_ERR_TIMEOUT in a device word, finishes
+ *     without further waiting and leaves garbage in y; sk_last_device_error()
+ *     reports it, and the workspace must then be re-created with sk_init().
+ */
+#ifndef SKINNY_H
+#define SKINNY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SK_API __attribute__((visibility("default")))
+#else
+#define SK_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SK_OK = 0,
+    SK_ERR_INVALID_ARG = 1,       /* NULL pointer, M outside 1..8, negative N/K */
+    SK_ERR_UNSUPPORTED_SHAPE = 2, /* K not a multiple of 256 (NVFP4) / 128 (FP8), or N too large */
+    SK_ERR_MISALIGNED = 3,        /* a pointer breaks the alignment rule of its argument */
+    SK_ERR_NOT_INITIALIZED = 4,   /* no sk_init() on the current device */
+    SK_ERR_CUDA = 5,              /* a CUDA runtime call or launch failed */
+    SK_ERR_TIMEOUT = 6,           /* a bounded in-kernel wait ran out (sk_last_device_error) */
+    SK_ERR_WORKSPACE = 7          /* the workspace is too small for this call's partial sums */
+} sk_status;
+
+/*
+ * Allocate (cudaMalloc) and zero the workspace of the CURRENT device.
+ * workspace_bytes = 0 picks the default, 64 MiB, which covers the largest call
+ * below (N = 151936, K = 5120, M = 8 needs about 25 MB).  Calling it again on
+ * the same device frees and re-creates the workspace (wait for all work of the
+ * library on that device first).  Call it before capturing any CUDA graph.
+ * It also resolves cuTensorMapEncodeTiled from the driver.
+ */
+SK_API sk_status sk_init(size_t workspace_bytes);
+
+/* Free the workspaces of all devices (synchronises each device first). */
+SK_API sk_status sk_shutdown(void);
+
+/*
+ * NVFP4 weight-only linear, FP32 output y[M][N].
+ *   x        const f16 [M][K], 16-byte aligned
+ *   W_codes  const u8 [N][K/2], 16-byte aligned
+ *   W_scales const u8 [N][K/16], 16-byte aligned
+ *   W_gscale FP32 tensor scale (any finite value)
+ *   y        f32 [M][N], 4-byte aligned
+ *   1 <= M <= 8; N >= 0 (N = 0: nothing is launched); K >= 0 with
+ *   K % 256 == 0 (K = 0: y is set to zero).
+ */
+SK_API sk_status nvfp4_gemm(const void *x, const uint8_t *W_codes, const uint8_t *W_scales,
+                     float W_gscale, float *y, int M, int N, int K, void *stream);
+
+/* As nvfp4_gemm, FP16 output (round to nearest even), y 2-byte aligned. */
+SK_API sk_status nvfp4_gemm_f16out(const void *x, const uint8_t *W_codes, const uint8_t *W_scales,
+                            float W_gscale, void *y, int M, int N, int K, void *stream);
+
+/*
+ * FP8-E4M3 weight-only linear with FP32 128x128 block scales, FP32 output.
+ *   x        const f16 [M][K], 16-byte aligned
+ *   W_codes  const u8 [N][K], 16-byte aligned
+ *   W_scales const f32 [ceil(N/128)][ceil(K/128)], 4-byte aligned
+ *   y        f32 [M][N], 4-byte aligned
+ *   1 <= M <= 8; N >= 0; K >= 0 with K % 128 == 0.
+ */
+SK_API sk_status fp8_gemm(const void *x, const uint8_t *W_codes, const float *W_scales,
+                   float *y, int M, int N, int K, void *stream);
+
+/* As fp8_gemm, FP16 output, y 2-byte aligned. */
+SK_API sk_status fp8_gemm_f16out(const void *x, const uint8_t *W_codes, const float *W_scales,
+                          void *y, int M, int N, int K, void *stream);
+
+/*
+ * NVFP4 vocabulary projection with a fused greedy pick: the logits are those
+ * of nvfp4_gemm and argmax[m] is the lowest n holding the maximum of row m of
+ * those same FP32 logits (the greedy / local-argmax proposal that the
+ * speculative verify round compares against, page "NVFP4 在 Volta 上！",
+ * section "这是一个服务器，不是 GEMM 截图"; native 4-bit lm_head, kernel table).
+ *   logits  f32 [M][N] or NULL (then only argmax is written)
+ *   argmax  i32 [M], 4-byte aligned
+ *   Other arguments as nvfp4_gemm; N >= 1.  NaN logits (not produced by
+ *   finite inputs) would order above +inf.
+ */
+SK_API sk_status lm_head_argmax(const void *x, const uint8_t *W_codes, const uint8_t *W_scales,
+                         float W_gscale, float *logits, int32_t *argmax,
+                         int M, int N, int K, void *stream);
+
+/* Static, human-readable name of a status code. */
+SK_API const char *sk_status_string(sk_status status);
+
+/*
+ * Wait for `stream`, then read and clear the device error word of the current
+ * device: SK_ERR_TIMEOUT if a kernel's bounded wait ran out since the last
+ * call, SK_OK otherwise (SK_ERR_CUDA if the synchronisation itself failed).
+ */
+SK_API sk_status sk_last_device_error(void *stream);
+
+/*
+ * Programmatic dependent launch between consecutive calls on one stream:
+ * 1 = on (default), 0 = off.  Process-wide; returns the previous setting.
+ */
+SK_API int sk_set_pdl(int enable);
+
+/*
+ * Failure-injection hook for tests: with enable = 1 the next kernel launched
+ * by this process on any device issues no weight copies, so its consumers'
+ * bounded waits run out (about one second); the kernel then finishes without
+ * further waiting and records SK_ERR_TIMEOUT, which sk_last_device_error()
+ * returns.  The hook clears itself after that one launch.  No fault, trap or
+ * unbounded wait is involved.
+ */
+SK_API void sk_inject_wait_timeout(int enable);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+SK_API int sk_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SKINNY_H */

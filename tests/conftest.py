@@ -15,3 +15,18 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return os.path.join(ROOT, "tests", "golden")
+
+
+def pytest_sessionstart(session):
+    # Build libskinny.so (nvcc, sm_103a) and the oracle (gcc) if they are
+    # missing or older than their sources; both builds are incremental.
+    import importlib.util
+
+    spec = importlib.util.spec_from_file_location(
+        "_skinny_build", os.path.join(ROOT, "fp8_weight_only_skinny_gb300", "build.py"))
+    skbuild = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(skbuild)   # without importing the package (it loads the .so)
+    skbuild.build()
+    import oracle
+
+    oracle.build()

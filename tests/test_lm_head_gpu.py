@@ -1,0 +1,85 @@
+"""GPU parity of the NVFP4 lm_head with the fused greedy argmax."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import check, dev, host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sk():
+    import torch
+
+    torch.cuda.set_device(0)
+    import fp8_weight_only_skinny_gb300 as skm
+
+    skm.init()
+    yield skm
+    assert skm.last_device_error() == skm.SK_OK
+
+
+def _argmax_ok(am, y_ref, l1, logits_gpu):
+    """The fused index is the lowest-index max of the same call's FP32 logits
+    (bitwise), and agrees with the oracle where its top-2 gap exceeds the bound."""
+    M = y_ref.shape[0]
+    tol = oracle.tolerance(l1)
+    for m in range(M):
+        assert am[m] == int(np.argmax(logits_gpu[m])), m
+        a = int(oracle.argmax_rows(y_ref[m:m + 1])[0])
+        order = np.argsort(-y_ref[m], kind="stable")
+        b = int(order[1]) if order[0] == a else int(order[0])
+        if y_ref[m, a] - y_ref[m, b] > tol[m, a] + tol[m, b]:
+            assert am[m] == a, (m, am[m], a)
+        else:
+            i = am[m]
+            assert y_ref[m, i] >= y_ref[m, a] - tol[m, a] - tol[m, i]
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8])
+@pytest.mark.parametrize("K,N", [(1024, 4099), (5120, 3000), (256, 16)])
+def test_lm_head_logits_and_argmax(sk, M, K, N):
+    x = synth.x_f16(M, K, seed=M * 31 + N)
+    codes, scales, g = synth.nvfp4_weights(N, K, seed=N)
+    y_ref, l1 = oracle.nvfp4_linear(x, codes, scales, g)
+    logits, am = sk.lm_head_argmax(dev(x), dev(codes), dev(scales), float(g))
+    lg = host(logits)
+    check(lg, y_ref, l1, False, "lm_head logits")
+    _argmax_ok(host(am), y_ref, l1, lg)
+    # without logits: same indices
+    _, am2 = sk.lm_head_argmax(dev(x), dev(codes), dev(scales), float(g), want_logits=False)
+    assert np.array_equal(host(am2), host(am))
+
+
+def test_ties_go_to_the_lowest_index(sk):
+    M, K, N = 8, 1024, 700
+    x = synth.x_f16(M, K, seed=5)
+    codes, scales, g = synth.nvfp4_weights(N, K, seed=5)
+    y_ref, _ = oracle.nvfp4_linear(x, codes, scales, g)
+    # copy each row's winner to a later and an earlier row: the earliest copy wins
+    win = oracle.argmax_rows(y_ref)
+    codes2, scales2 = codes.copy(), scales.copy()
+    for m in range(M):
+        for dst in (3 + 80 * m, N - 1 - m):
+            codes2[dst], scales2[dst] = codes[win[m]], scales[win[m]]
+    y2, _ = oracle.nvfp4_linear(x, codes2, scales2, g)
+    logits, am = sk.lm_head_argmax(dev(x), dev(codes2), dev(scales2), float(g))
+    lg, am = host(logits), host(am)
+    for m in range(M):
+        assert am[m] == int(np.argmax(lg[m]))
+        assert lg[m, am[m]] == lg[m].max()
+
+
+def test_repeated_argmax_is_stable(sk):
+    M, K, N = 8, 2048, 9001
+    x = synth.x_f16(M, K, seed=9)
+    codes, scales, g = synth.nvfp4_weights(N, K, seed=9)
+    first = None
+    for _ in range(5):
+        logits, am = sk.lm_head_argmax(dev(x), dev(codes), dev(scales), float(g))
+        cur = (host(logits), host(am))
+        if first is None:
+            first = cur
+        assert np.array_equal(cur[0], first[0]) and np.array_equal(cur[1], first[1])
