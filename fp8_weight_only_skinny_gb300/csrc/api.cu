@@ -78,8 +78,21 @@ int padded_m(int M) {
     return 8;
 }
 
+// Persistent grid: CTAS_PER_SM CTAs per SM, never more CTAs than units.
+// SK_CTAS_PER_SM (1..4) overrides the CTAs per SM; SK_MAX_CTAS caps the grid,
+// which the tests use to give every CTA many units on small shapes (ring
+// wrap-around, k-chunk changes and multi-unit fix-ups).
 int grid_for(const DeviceState *d, long long units) {
-    long long g = d->num_sms > 0 ? d->num_sms : 1;
+    int per_sm = 2;
+    if (const char *e = std::getenv("SK_CTAS_PER_SM")) {
+        const int v = std::atoi(e);
+        if (v >= 1 && v <= 4) per_sm = v;
+    }
+    long long g = (long long)(d->num_sms > 0 ? d->num_sms : 1) * per_sm;
+    if (const char *e = std::getenv("SK_MAX_CTAS")) {
+        const long long v = std::atoll(e);
+        if (v >= 1 && v < g) g = v;
+    }
     return int(units < g ? units : g);
 }
 

@@ -48,6 +48,8 @@ constexpr int NGROUPS = 2;        // consumer groups per CTA
 constexpr int GROUP_THREADS = 128;
 constexpr int CTA_THREADS = NGROUPS * GROUP_THREADS + 32;   // + one producer warp
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;            // bounded waits: ~1 s
+// flags: [0] abort, [2] fix-up list length, [16 .. 16 + consumer threads) fix-up list
+constexpr int FLAG_BYTES = 64 + 4 * NGROUPS * GROUP_THREADS;
 
 // Workspace layout (bytes): control block, row-group counters, partial sums.
 constexpr size_t WS_CTRL_BYTES = 4096;
@@ -83,6 +85,13 @@ template <> struct Traits<FP8> {
     static constexpr int SCALE_BOX_X = 0;
 };
 
+// Consecutive uses of a ring stage must go to the same consumer group: stage
+// s then always serves units i = s (mod STAGES) of group s % NGROUPS, which that
+// group consumes in order, so a waiter can never see a parity left over from
+// a stage use two phases back.
+static_assert(Traits<NVFP4>::STAGES % NGROUPS == 0, "ring stages must be a multiple of NGROUPS");
+static_assert(Traits<FP8>::STAGES % NGROUPS == 0, "ring stages must be a multiple of NGROUPS");
+
 struct Params {
     const __half *x;            // [M][K]
     const float *fp8_scales;    // FP8: [ceil(N/128)][KB]
@@ -96,14 +105,15 @@ struct Params {
     int stall;                  // failure injection: the producer issues no copies
 };
 
-template <int FMT, int MP>
+// Floats of a group's per-unit reduction buffer: MMA = 4 warps x (16 rows x 8
+// tokens), SIMT = 16 rows x MP.
+template <int MP>
 __host__ __device__ constexpr int red_floats() { return MP == 8 ? 4 * 128 : RG * MP; }
 
 template <int FMT, int MP>
 __host__ __device__ constexpr size_t smem_bytes() {
-    return 1024 + size_t(Traits<FMT>::STAGES) * Traits<FMT>::STAGE_BYTES +
-           16 * Traits<FMT>::STAGES + NGROUPS * red_floats<FMT, MP>() * 4 + 64 +
-           NGROUPS * GROUP_THREADS * 8;
+    return 1024 + size_t(Traits<FMT>::STAGES) * Traits<FMT>::STAGE_BYTES + 16 * Traits<FMT>::STAGES +
+           NGROUPS * red_floats<MP>() * 4 + FLAG_BYTES + NGROUPS * GROUP_THREADS * 8;
 }
 
 // Bounded mbarrier wait.  Gives up when the CTA's abort flag is set or after
@@ -240,30 +250,27 @@ __device__ __forceinline__ void unit_mma(float (&d)[4], const XRegs<FMT, 8> &xr,
             const uint4 A = ld_shared_v4(codes + r * 512 + off);
             const uint4 B = ld_shared_v4(codes + (r + 8) * 512 + off);
             const uint32_t soff = 16 * w + 8 * t + 2 * q;
-            const uint32_t sa = e4m3x2_to_f16x2<0>(ld_shared_u16(scales + r * 64 + soff));
-            const uint32_t sb = e4m3x2_to_f16x2<0>(ld_shared_u16(scales + (r + 8) * 64 + soff));
+            const uint32_t sa = e4m3x2_h_to_f16x2(ld_shared_u16(scales + r * 64 + soff));
+            const uint32_t sb = e4m3x2_h_to_f16x2(ld_shared_u16(scales + (r + 8) * 64 + soff));
             const uint32_t sa0 = bcast_lo(sa), sa1 = bcast_hi(sa);
             const uint32_t sb0 = bcast_lo(sb), sb1 = bcast_hi(sb);
             const uint32_t Aw[4] = {A.x, A.y, A.z, A.w};
             const uint32_t Bw[4] = {B.x, B.y, B.z, B.w};
 #pragma unroll
-            for (int ii = 0; ii < 8; ++ii) {
-                const uint32_t wa = Aw[ii >> 1], wb = Bw[ii >> 1];
-                const uint32_t s_a = ii < 4 ? sa0 : sa1;
-                const uint32_t s_b = ii < 4 ? sb0 : sb1;
-                uint32_t a0, a1, a2, a3;
-                if (ii & 1) {
-                    a0 = hmul2(e2m1x2_to_f16x2<2>(wa), s_a);
-                    a1 = hmul2(e2m1x2_to_f16x2<2>(wb), s_b);
-                    a2 = hmul2(e2m1x2_to_f16x2<3>(wa), s_a);
-                    a3 = hmul2(e2m1x2_to_f16x2<3>(wb), s_b);
-                } else {
-                    a0 = hmul2(e2m1x2_to_f16x2<0>(wa), s_a);
-                    a1 = hmul2(e2m1x2_to_f16x2<0>(wb), s_b);
-                    a2 = hmul2(e2m1x2_to_f16x2<1>(wa), s_a);
-                    a3 = hmul2(e2m1x2_to_f16x2<1>(wb), s_b);
+            for (int wd = 0; wd < 4; ++wd) {
+                // word wd = bytes 4wd..4wd+3 = k steps ii = 2wd (bytes 0,1) and 2wd+1 (bytes 2,3)
+                uint32_t da[4], db[4];
+                e2m1x8_to_f16x2x4(Aw[wd], da);
+                e2m1x8_to_f16x2x4(Bw[wd], db);
+                const uint32_t s_a = wd < 2 ? sa0 : sa1;
+                const uint32_t s_b = wd < 2 ? sb0 : sb1;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int ii = 2 * wd + h;
+                    mma_16816(acc[ii & 1], hmul2(da[2 * h], s_a), hmul2(db[2 * h], s_b),
+                              hmul2(da[2 * h + 1], s_a), hmul2(db[2 * h + 1], s_b),
+                              xr.w[0][t][2 * ii], xr.w[0][t][2 * ii + 1]);
                 }
-                mma_16816(acc[ii & 1], a0, a1, a2, a3, xr.w[0][t][2 * ii], xr.w[0][t][2 * ii + 1]);
             }
         }
 #pragma unroll
@@ -280,9 +287,10 @@ __device__ __forceinline__ void unit_mma(float (&d)[4], const XRegs<FMT, 8> &xr,
             const uint32_t Bw[4] = {B.x, B.y, B.z, B.w};
 #pragma unroll
             for (int ii = 0; ii < 4; ++ii) {
-                mma_16816(acc[t >> 1], e4m3x2_to_f16x2<0>(Aw[ii]), e4m3x2_to_f16x2<0>(Bw[ii]),
-                          e4m3x2_to_f16x2<1>(Aw[ii]), e4m3x2_to_f16x2<1>(Bw[ii]),
-                          xr.w[0][t][2 * ii], xr.w[0][t][2 * ii + 1]);
+                uint32_t a0, a2, a1, a3;
+                e4m3x4_to_f16x2x2(Aw[ii], a0, a2);
+                e4m3x4_to_f16x2x2(Bw[ii], a1, a3);
+                mma_16816(acc[t >> 1], a0, a1, a2, a3, xr.w[0][t][2 * ii], xr.w[0][t][2 * ii + 1]);
             }
         }
         const int rb = g >> 3;                  // 128-row block of this row group
@@ -306,24 +314,23 @@ __device__ __forceinline__ void unit_simt(float (&out)[4 * MP], const XRegs<FMT,
         for (int i = 0; i < 4; ++i) {
             const int row = 4 * w + i;
             const uint4 A = ld_shared_v4(codes + row * 512 + 16 * lane);
-            const float2 sf = f16x2_to_f32x2(e4m3x2_to_f16x2<0>(ld_shared_u16(scales + row * 64 + 2 * lane)));
+            const float2 sf = f16x2_to_f32x2(e4m3x2_h_to_f16x2(ld_shared_u16(scales + row * 64 + 2 * lane)));
             const uint32_t Aw[4] = {A.x, A.y, A.z, A.w};
             float b0[MP], b1[MP];
 #pragma unroll
             for (int m = 0; m < MP; ++m) { b0[m] = 0.f; b1[m] = 0.f; }
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                uint32_t wv;
-                switch (j & 3) {
-                    case 0: wv = e2m1x2_to_f16x2<0>(Aw[j >> 2]); break;
-                    case 1: wv = e2m1x2_to_f16x2<1>(Aw[j >> 2]); break;
-                    case 2: wv = e2m1x2_to_f16x2<2>(Aw[j >> 2]); break;
-                    default: wv = e2m1x2_to_f16x2<3>(Aw[j >> 2]); break;
-                }
+            for (int wd = 0; wd < 4; ++wd) {
+                uint32_t dw[4];
+                e2m1x8_to_f16x2x4(Aw[wd], dw);
 #pragma unroll
-                for (int m = 0; m < MP; ++m) {
-                    if (j < 8) b0[m] = fma2_f16_f32(wv, xr.w[m][0][j], b0[m]);
-                    else       b1[m] = fma2_f16_f32(wv, xr.w[m][0][j], b1[m]);
+                for (int bb = 0; bb < 4; ++bb) {
+                    const int j = 4 * wd + bb;
+#pragma unroll
+                    for (int m = 0; m < MP; ++m) {
+                        if (j < 8) b0[m] = fma2_f16_f32(dw[bb], xr.w[m][0][j], b0[m]);
+                        else       b1[m] = fma2_f16_f32(dw[bb], xr.w[m][0][j], b1[m]);
+                    }
                 }
             }
 #pragma unroll
@@ -346,12 +353,18 @@ __device__ __forceinline__ void unit_simt(float (&out)[4 * MP], const XRegs<FMT,
 #pragma unroll
             for (int m = 0; m < MP; ++m) { p0[m] = 0.f; p1[m] = 0.f; }
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const uint32_t wv = (j & 1) ? e4m3x2_to_f16x2<1>(Aw[j >> 1]) : e4m3x2_to_f16x2<0>(Aw[j >> 1]);
+            for (int wd = 0; wd < 8; ++wd) {
+                uint32_t wlo, whi;
+                e4m3x4_to_f16x2x2(Aw[wd], wlo, whi);
 #pragma unroll
                 for (int m = 0; m < MP; ++m) {
-                    if (j < 8) p0[m] = fma2_f16_f32(wv, xr.w[m][0][j], p0[m]);
-                    else       p1[m] = fma2_f16_f32(wv, xr.w[m][0][j], p1[m]);
+                    if (wd < 4) {
+                        p0[m] = fma2_f16_f32(wlo, xr.w[m][0][2 * wd], p0[m]);
+                        p0[m] = fma2_f16_f32(whi, xr.w[m][0][2 * wd + 1], p0[m]);
+                    } else {
+                        p1[m] = fma2_f16_f32(wlo, xr.w[m][0][2 * wd], p1[m]);
+                        p1[m] = fma2_f16_f32(whi, xr.w[m][0][2 * wd + 1], p1[m]);
+                    }
                 }
             }
 #pragma unroll
@@ -360,14 +373,44 @@ __device__ __forceinline__ void unit_simt(float (&out)[4 * MP], const XRegs<FMT,
     }
 }
 
+// Write output o (row o / MP, token o % MP) of row group g; track the best
+// argmax key of this thread's token.
+template <int FMT, int MP, bool F16OUT, bool ARGMAX>
+__device__ __forceinline__ void finalize(const Params &p, int g, int o, float v, unsigned long long &best) {
+    const int row = o / MP, m = o % MP;
+    const int n = g * RG + row;
+    const float val = (FMT == NVFP4) ? v * p.gscale : v;
+    if (n < p.N && m < p.M) {
+        if (p.y) {
+            if constexpr (F16OUT) reinterpret_cast<__half *>(p.y)[size_t(m) * p.N + n] = __float2half_rn(val);
+            else reinterpret_cast<float *>(p.y)[size_t(m) * p.N + n] = val;
+        }
+        if constexpr (ARGMAX) {
+            const unsigned long long key =
+                (static_cast<unsigned long long>(ordered_bits(val)) << 32) | static_cast<unsigned int>(~n);
+            best = key > best ? key : best;
+        }
+    }
+}
+
 // ----------------------------------------------------------------------------
+// CTA roles: warps 0 .. 4*NGROUPS-1 are consumers (unit i goes to group
+// i % NGROUPS, whose four warps split its k-chunk or its rows); the last warp
+// is the producer, one lane of which issues the TMA loads.  Per unit a group
+// reduces its warps' partial sums through shared memory and either writes y
+// (one k-chunk) or stores the unit's split-K partial with a plain store.  The
+// counter atomics that find the last contributor of each row group, and the
+// sums of the C partials in ascending chunk order, run once per CTA after its
+// whole range, by all consumer threads in parallel: no global round trip sits
+// on the per-unit path.
 template <int FMT, int MP, bool F16OUT, bool ARGMAX>
 __global__ void __launch_bounds__(CTA_THREADS, 2)
 skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
               const Params p) {
     using T = Traits<FMT>;
-    constexpr int RED = red_floats<FMT, MP>();
+    constexpr int RED = red_floats<MP>();
     constexpr int NOUT = RG * MP;                 // outputs per unit
+    constexpr int CT = NGROUPS * GROUP_THREADS;   // consumer threads
 
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -376,9 +419,10 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
     const uint32_t bar_full = base + T::STAGES * T::STAGE_BYTES;
     const uint32_t bar_empty = bar_full + 8 * T::STAGES;
     float *red = reinterpret_cast<float *>(sb + T::STAGES * T::STAGE_BYTES + 16 * T::STAGES);
-    volatile int *flags = reinterpret_cast<volatile int *>(red + NGROUPS * RED);   // [0] abort, [1+q] last
+    volatile int *flags = reinterpret_cast<volatile int *>(red + NGROUPS * RED);
+    int *fix_list = const_cast<int *>(flags) + 16;            // CT entries
     unsigned long long *keys = reinterpret_cast<unsigned long long *>(
-        sb + T::STAGES * T::STAGE_BYTES + 16 * T::STAGES + NGROUPS * RED * 4 + 64);
+        sb + T::STAGES * T::STAGE_BYTES + 16 * T::STAGES + NGROUPS * RED * 4 + FLAG_BYTES);
 
     Ctrl *ctrl = reinterpret_cast<Ctrl *>(p.ws);
     unsigned int *counters = reinterpret_cast<unsigned int *>(p.ws + WS_CTRL_BYTES);
@@ -439,11 +483,12 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
     // ------------------------------------------------------------ consumers ---
     const int q = warp >> 2, w = warp & 3;
     const int t = threadIdx.x - q * GROUP_THREADS;     // 0..127 within the group
+    const int ct = threadIdx.x;                        // 0..CT-1; token of this thread: ct % MP
     const uint32_t bar_id = 1 + q;
     float *gred = red + q * RED;
-    unsigned long long best = 0;                       // ARGMAX: best key of token t % MP
+    unsigned long long best = 0;                       // ARGMAX: best key of token ct % MP
 
-    pdl_wait_primary();
+    pdl_wait_primary();   // x, y and the workspace belong to the previous kernel until here
 
     XRegs<FMT, MP> xr;
     int cur_c = -1;
@@ -473,76 +518,63 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
             if (lane == 0) mbar_arrive(bar_empty + 8 * s);
             warp_reduce_split<4 * MP>(out, lane);
             constexpr int NV = 4 * MP;
-            // lanes holding a distinct value: the lowest lane of each run
-            const int idx = reduce_index<NV>(lane);
+            const int idx = reduce_index<NV>(lane);    // lanes holding a distinct value
             if ((lane & ((32 / NV) - 1)) == 0) gred[(4 * w) * MP + idx] = out[0];
         }
         named_bar_sync(bar_id, GROUP_THREADS);
 
-        // value of output t of this unit (row t / MP, token t % MP)
-        float v = 0.f;
+        // output t of this unit: row t / MP, token t % MP
         if (t < NOUT) {
+            float v;
             if constexpr (MP == 8) v = gred[t] + gred[128 + t] + gred[256 + t] + gred[384 + t];
             else v = gred[t];
+            if (p.C == 1) finalize<FMT, MP, F16OUT, ARGMAX>(p, g, t, v, best);
+            else partials[((size_t)g * p.C + c) * NOUT + t] = v;   // plain store
         }
-        bool final_here = (p.C == 1);
-        if (!final_here) {
-            if (t < NOUT) partials[((size_t)g * p.C + c) * NOUT + t] = v;
-            __threadfence();
-            named_bar_sync(bar_id, GROUP_THREADS);
-            if (t == 0) {
-                const unsigned int old = atomicAdd(counters + g, 1u);
-                flags[1 + q] = (old == unsigned(p.C - 1));
+        named_bar_sync(bar_id, GROUP_THREADS);   // gred is reused by the next unit
+    }
+
+    if (p.C > 1) {
+        // Split-K fix-up: one counter atomic per unit of this CTA, CT at a time;
+        // the CTA whose atomic completes a row group sums its C partials.
+        int *fix_n = const_cast<int *>(flags) + 2;
+        __threadfence();                               // release this thread's partials
+        for (int b0 = 0; b0 < n_units; b0 += CT) {
+            if (ct == 0) *fix_n = 0;
+            named_bar_sync(15, CT);
+            const int i = b0 + ct;
+            if (i < n_units) {
+                const int g = int((u_lo + i) % p.G);
+                if (atomicAdd(counters + g, 1u) == unsigned(p.C - 1)) fix_list[atomicAdd(fix_n, 1)] = g;
             }
-            named_bar_sync(bar_id, GROUP_THREADS);
-            final_here = flags[1 + q] != 0;
-            if (final_here) {
-                __threadfence();
-                if (t < NOUT) {
-                    const float *src = partials + (size_t)g * p.C * NOUT + t;
-                    float acc = ld_cg_f32(src);
-                    for (int cc = 1; cc < p.C; ++cc) acc += ld_cg_f32(src + (size_t)cc * NOUT);
-                    v = acc;
-                }
-                if (t == 0) counters[g] = 0u;
+            named_bar_sync(15, CT);
+            const int n_fix = *fix_n;
+            __threadfence();                           // acquire the other CTAs' partials
+            for (int e = ct / NOUT; e < n_fix; e += CT / NOUT) {
+                const int g = fix_list[e], o = ct % NOUT;
+                const float *src = partials + (size_t)g * p.C * NOUT + o;
+                float acc = ld_cg_f32(src);
+                for (int cc = 1; cc < p.C; ++cc) acc += ld_cg_f32(src + (size_t)cc * NOUT);
+                finalize<FMT, MP, F16OUT, ARGMAX>(p, g, o, acc, best);
             }
-        } else {
-            named_bar_sync(bar_id, GROUP_THREADS);   // gred is reused by the next unit
-        }
-        if (final_here && t < NOUT) {
-            const int row = t / MP, m = t % MP;
-            const int n = g * RG + row;
-            const float val = (FMT == NVFP4) ? v * p.gscale : v;
-            if (n < p.N && m < p.M) {
-                if (p.y) {
-                    if constexpr (F16OUT) reinterpret_cast<__half *>(p.y)[size_t(m) * p.N + n] = __float2half_rn(val);
-                    else reinterpret_cast<float *>(p.y)[size_t(m) * p.N + n] = val;
-                }
-                if constexpr (ARGMAX) {
-                    const unsigned long long key =
-                        (static_cast<unsigned long long>(ordered_bits(val)) << 32) | static_cast<unsigned int>(~n);
-                    best = key > best ? key : best;
-                }
-            }
+            if (ct < n_fix) counters[fix_list[ct]] = 0u;
+            named_bar_sync(15, CT);
         }
     }
 
     if constexpr (ARGMAX) {
         // Per-CTA best per token -> one 64-bit atomicMax per token; the last CTA
         // to finish turns the keys into indices and resets them.
-        keys[q * GROUP_THREADS + t] = best;
-        named_bar_sync(15, NGROUPS * GROUP_THREADS);
-        if (q == 0 && t < MP) {
+        keys[ct] = best;
+        named_bar_sync(15, CT);
+        if (ct < MP) {
             unsigned long long k = 0;
-            for (int e = t; e < NGROUPS * GROUP_THREADS; e += MP) {
-                const int te = e % GROUP_THREADS;
-                if (te < NOUT) k = keys[e] > k ? keys[e] : k;
-            }
-            if (k != 0 && t < p.M) atomicMax(&ctrl->argmax_key[t], k);
+            for (int e = ct; e < CT; e += MP) k = keys[e] > k ? keys[e] : k;
+            if (k != 0 && ct < p.M) atomicMax(&ctrl->argmax_key[ct], k);
             __threadfence();
         }
-        named_bar_sync(15, NGROUPS * GROUP_THREADS);
-        if (q == 0 && t == 0) {
+        named_bar_sync(15, CT);
+        if (ct == 0) {
             const unsigned int old = atomicAdd(&ctrl->done, 1u);
             if (old == gridDim.x - 1) {
                 __threadfence();

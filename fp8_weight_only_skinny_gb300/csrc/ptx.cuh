@@ -86,21 +86,27 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
 
 // ------------------------------------------------------------ decoders -----
 
-// Byte `B` of `w` (two E2M1 codes, low nibble first) -> f16x2 {low, high}.
-template <int B>
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t w) {
-    uint32_t d;
-    asm("{ .reg .b8 t; .reg .b32 s; shr.u32 s, %1, %2; cvt.u8.u32 t, s; cvt.rn.f16x2.e2m1x2 %0, t; }"
-        : "=r"(d) : "r"(w), "n"(8 * B));
-    return d;
+// All four bytes of `w` (eight E2M1 codes, low nibble first) -> four f16x2;
+// d[b] holds the codes of byte b.  The vector unpack lets the converts read
+// the bytes in place (no shift per byte).
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&d)[4]) {
+    asm("{ .reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0; cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2; cvt.rn.f16x2.e2m1x2 %3, b3; }"
+        : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3]) : "r"(w));
 }
 
-// Half `H` of `w` (two E4M3 codes, low byte first) -> f16x2 {low, high}.
-template <int H>
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
+// Both halves of `w` (four E4M3 codes, low byte first) -> two f16x2.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    asm("{ .reg .b16 a, b; mov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a; cvt.rn.f16x2.e4m3x2 %1, b; }"
+        : "=r"(lo), "=r"(hi) : "r"(w));
+}
+
+// A 16-bit pair of E4M3 codes -> f16x2.
+__device__ __forceinline__ uint32_t e4m3x2_h_to_f16x2(uint16_t h) {
     uint32_t d;
-    asm("{ .reg .b16 t; .reg .b32 s; shr.u32 s, %1, %2; cvt.u16.u32 t, s; cvt.rn.f16x2.e4m3x2 %0, t; }"
-        : "=r"(d) : "r"(w), "n"(16 * H));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(h));
     return d;
 }
 
@@ -149,7 +155,7 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
     return v;
 }
 
-__device__ __forceinline__ uint32_t ld_shared_u16(uint32_t addr) {
+__device__ __forceinline__ uint16_t ld_shared_u16(uint32_t addr) {
     uint16_t v;
     asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
     return v;
