@@ -248,14 +248,16 @@ def oracle_pass(sample):
 
 
 def size_oracle_sample(M, budget_s):
-    """Double the sampled columns until one oracle pass takes >= budget_s."""
-    cols = 32
+    """Grow the sampled columns until one oracle pass takes >= budget_s (at most
+    one extrapolated jump after a small timing pass; capped at 32768 columns)."""
+    cols = 64
     while True:
         sample = oracle_sample_inputs(M, cols)
         nbytes, dt = oracle_pass(sample)
-        if dt >= budget_s or cols >= 8192:
+        if dt >= budget_s or cols >= 32768:
             return sample, cols, nbytes, dt
-        cols *= 2
+        want = int(cols * budget_s / max(dt, 1e-3) * 1.1) + 1
+        cols = min(32768, max(cols * 2, want))
 
 
 def cpu_oracle_sample(M, budget_s=10.0):
