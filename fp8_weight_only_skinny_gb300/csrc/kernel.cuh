@@ -136,6 +136,16 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
     }
 }
 
+// Advance unit (c, g) by `by` units in chunk-major order (u = c * G + g),
+// without a division per unit (the loop runs more than once only when G < by).
+__device__ __forceinline__ void step_unit(int &c, int &g, int by, int G) {
+    g += by;
+    while (g >= G) {
+        g -= G;
+        c += 1;
+    }
+}
+
 // Order-preserving map of an FP32 value to u32 (larger value -> larger key).
 __device__ __forceinline__ unsigned int ordered_bits(float v) {
     unsigned int u = __float_as_uint(v);
@@ -432,6 +442,7 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
     const long long u_lo = (long long)blockIdx.x * p.U / gridDim.x;
     const long long u_hi = (long long)(blockIdx.x + 1) * p.U / gridDim.x;
     const int n_units = int(u_hi - u_lo);
+    const int c_lo = int(u_lo / p.G), g_lo = int(u_lo % p.G);   // first unit of the range
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < T::STAGES; ++s) {
@@ -451,13 +462,12 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
         if (lane == 0) {
             const uint64_t pol = l2_evict_first_policy();
             int issued = 0;
-            for (int i = 0; i < (p.stall ? 0 : n_units); ++i) {
+            int c = c_lo, g = g_lo;                        // unit u_lo + i, stepped without division
+            for (int i = 0; i < (p.stall ? 0 : n_units); ++i, step_unit(c, g, 1, p.G)) {
                 const int s = i % T::STAGES;
                 if (i >= T::STAGES &&
                     !wait_bounded(bar_empty + 8 * s, ((i / T::STAGES) & 1) ^ 1, flags, &ctrl->err))
                     break;
-                const long long u = u_lo + i;
-                const int c = int(u / p.G), g = int(u % p.G);
                 const uint32_t dst = base + s * T::STAGE_BYTES;
                 mbar_arrive_expect_tx(bar_full + 8 * s, T::STAGE_BYTES);
                 tma_load_2d(dst, &tm_codes, bar_full + 8 * s, c * T::CODE_BOX_X, g * RG, pol);
@@ -492,9 +502,9 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
 
     XRegs<FMT, MP> xr;
     int cur_c = -1;
-    for (int i = q; i < n_units; i += NGROUPS) {
-        const long long u = u_lo + i;
-        const int c = int(u / p.G), g = int(u % p.G);
+    int c = c_lo, g = g_lo;
+    step_unit(c, g, q, p.G);                           // unit u_lo + q
+    for (int i = q; i < n_units; i += NGROUPS, step_unit(c, g, NGROUPS, p.G)) {
         if (c != cur_c) {
             load_x<FMT, MP>(xr, p, c, w, lane);
             cur_c = c;
@@ -544,7 +554,7 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
             named_bar_sync(15, CT);
             const int i = b0 + ct;
             if (i < n_units) {
-                const int g = int((u_lo + i) % p.G);
+                const int g = int((u_lo + i) % p.G);      // once per unit, after the stream
                 if (atomicAdd(counters + g, 1u) == unsigned(p.C - 1)) fix_list[atomicAdd(fix_n, 1)] = g;
             }
             named_bar_sync(15, CT);
