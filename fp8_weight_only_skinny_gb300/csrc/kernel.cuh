@@ -560,12 +560,27 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
             named_bar_sync(15, CT);
             const int n_fix = *fix_n;
             __threadfence();                           // acquire the other CTAs' partials
-            for (int e = ct / NOUT; e < n_fix; e += CT / NOUT) {
-                const int g = fix_list[e], o = ct % NOUT;
-                const float *src = partials + (size_t)g * p.C * NOUT + o;
-                float acc = ld_cg_f32(src);
-                for (int cc = 1; cc < p.C; ++cc) acc += ld_cg_f32(src + (size_t)cc * NOUT);
-                finalize<FMT, MP, F16OUT, ARGMAX>(p, g, o, acc, best);
+            // Thread ct sums output o of row groups fix_list[e0], [e0 + ES], ...;
+            // four row groups at a time so that their loads are in flight together.
+            constexpr int ES = CT / NOUT;
+            const int o = ct % NOUT;
+            for (int e = ct / NOUT; e < n_fix; e += 4 * ES) {
+                int gg[4];
+                float acc[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    gg[j] = e + j * ES < n_fix ? fix_list[e + j * ES] : -1;
+                    acc[j] = 0.f;
+                }
+#pragma unroll 4
+                for (int cc = 0; cc < p.C; ++cc) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (gg[j] >= 0) acc[j] += ld_cg_f32(partials + ((size_t)gg[j] * p.C + cc) * NOUT + o);
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (gg[j] >= 0) finalize<FMT, MP, F16OUT, ARGMAX>(p, gg[j], o, acc[j], best);
             }
             if (ct < n_fix) counters[fix_list[ct]] = 0u;
             named_bar_sync(15, CT);

@@ -169,6 +169,18 @@ __device__ __forceinline__ uint4 ld_global_v4(const void *p) {
     return v;
 }
 
+// Acquire load at GPU scope (pairs with the fence + atomic of the writer).
+__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int *p) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Bring the line holding `p` into L1 (no register, no wait).
+__device__ __forceinline__ void prefetch_l1(const void *p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 // Coherent-at-L2 load for data written by other CTAs of the same grid.
 __device__ __forceinline__ float ld_cg_f32(const float *p) {
     float v;
