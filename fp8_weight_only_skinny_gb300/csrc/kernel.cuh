@@ -429,8 +429,7 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
     const uint32_t bar_full = base + T::STAGES * T::STAGE_BYTES;
     const uint32_t bar_empty = bar_full + 8 * T::STAGES;
     float *red = reinterpret_cast<float *>(sb + T::STAGES * T::STAGE_BYTES + 16 * T::STAGES);
-    volatile int *flags = reinterpret_cast<volatile int *>(red + NGROUPS * RED);
-    int *fix_list = const_cast<int *>(flags) + 16;            // CT entries
+    volatile int *flags = reinterpret_cast<volatile int *>(red + NGROUPS * RED);   // [0] abort
     unsigned long long *keys = reinterpret_cast<unsigned long long *>(
         sb + T::STAGES * T::STAGE_BYTES + 16 * T::STAGES + NGROUPS * RED * 4 + FLAG_BYTES);
 
@@ -544,24 +543,25 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
         named_bar_sync(bar_id, GROUP_THREADS);   // gred is reused by the next unit
     }
 
-    if (p.C > 1) {
-        // Split-K fix-up: one counter atomic per unit of this CTA, CT at a time;
-        // the CTA whose atomic completes a row group sums its C partials.
+    if (MP != 8 && p.C > 1) {
+        // Split-K fix-up, SIMT variants (few outputs per row group): one counter
+        // atomic per unit of this CTA, CT at a time; the CTA whose atomic
+        // completes a row group sums its C partials in ascending chunk order.
+        // CTAs that complete nothing leave at once.
         int *fix_n = const_cast<int *>(flags) + 2;
+        int *fix_list = const_cast<int *>(flags) + 16;          // CT entries
         __threadfence();                               // release this thread's partials
         for (int b0 = 0; b0 < n_units; b0 += CT) {
             if (ct == 0) *fix_n = 0;
             named_bar_sync(15, CT);
             const int i = b0 + ct;
             if (i < n_units) {
-                const int g = int((u_lo + i) % p.G);      // once per unit, after the stream
+                const int g = int((u_lo + i) % p.G);
                 if (atomicAdd(counters + g, 1u) == unsigned(p.C - 1)) fix_list[atomicAdd(fix_n, 1)] = g;
             }
             named_bar_sync(15, CT);
             const int n_fix = *fix_n;
             __threadfence();                           // acquire the other CTAs' partials
-            // Thread ct sums output o of row groups fix_list[e0], [e0 + ES], ...;
-            // four row groups at a time so that their loads are in flight together.
             constexpr int ES = CT / NOUT;
             const int o = ct % NOUT;
             for (int e = ct / NOUT; e < n_fix; e += 4 * ES) {
@@ -585,6 +585,60 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
             if (ct < n_fix) counters[fix_list[ct]] = 0u;
             named_bar_sync(15, CT);
         }
+    }
+
+    if (MP == 8 && p.C > 1) {
+        // Split-K fix-up, MMA variant (128 outputs per row group: the sums are
+        // the heavy part, so they are shared out evenly).  (1) Publish: every thread releases its partial stores,
+        // then one fire-and-forget counter increment per unit of this CTA.
+        // (2) Finish: row group g belongs to CTA g mod P (an even share for
+        // every CTA); it waits (bounded) until all C partials of each of its
+        // row groups are published and sums them in ascending chunk order.
+        __threadfence();
+        named_bar_sync(15, CT);
+        for (int i = ct; i < n_units; i += CT) atomicAdd(counters + int((u_lo + i) % p.G), 1u);
+        const int P = gridDim.x;
+        const int n_own = p.G > int(blockIdx.x) ? (p.G - 1 - int(blockIdx.x)) / P + 1 : 0;
+        if (ct == 0) {
+            const uint64_t t0 = globaltimer_ns();
+            for (int e = 0; e < n_own; ++e) {
+                const unsigned int *cnt = counters + int(blockIdx.x) + e * P;
+                while (ld_acquire_u32(cnt) != unsigned(p.C)) {
+                    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+                        flags[0] = 1;
+                        atomicOr(&ctrl->err, ERR_TIMEOUT);
+                        break;
+                    }
+                }
+                if (flags[0]) break;
+            }
+        }
+        named_bar_sync(15, CT);
+        __threadfence();                               // acquire the published partials
+        // Thread ct sums output o of owned row groups e0, e0 + ES, ...; four
+        // row groups at a time so that their loads are in flight together.
+        constexpr int ES = CT / NOUT;
+        const int o = ct % NOUT;
+        for (int e = ct / NOUT; e < n_own; e += 4 * ES) {
+            int gg[4];
+            float acc[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                gg[j] = e + j * ES < n_own ? int(blockIdx.x) + (e + j * ES) * P : -1;
+                acc[j] = 0.f;
+            }
+#pragma unroll 4
+            for (int cc = 0; cc < p.C; ++cc) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (gg[j] >= 0) acc[j] += ld_cg_f32(partials + ((size_t)gg[j] * p.C + cc) * NOUT + o);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (gg[j] >= 0) finalize<FMT, MP, F16OUT, ARGMAX>(p, gg[j], o, acc[j], best);
+        }
+        named_bar_sync(15, CT);
+        for (int e = ct; e < n_own; e += CT) counters[int(blockIdx.x) + e * P] = 0u;
     }
 
     if constexpr (ARGMAX) {
