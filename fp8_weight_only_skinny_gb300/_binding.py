@@ -50,6 +50,7 @@ def _load() -> ctypes.CDLL:
         "sk_set_pdl": ([i], i),
         "sk_version": ([], i),
         "sk_inject_wait_timeout": ([i], None),
+        "nvfp4_gemm_noalloc": ([p, p, p, f, p, i, i, i, p], i),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -63,7 +64,7 @@ lib = _load()
 # Names declared in include/skinny.h (the tests check that each is exported).
 EXPORTS = ("sk_init", "sk_shutdown", "nvfp4_gemm", "nvfp4_gemm_f16out", "fp8_gemm",
            "fp8_gemm_f16out", "lm_head_argmax", "sk_status_string", "sk_last_device_error",
-           "sk_set_pdl", "sk_inject_wait_timeout", "sk_version")
+           "sk_set_pdl", "sk_inject_wait_timeout", "nvfp4_gemm_noalloc", "sk_version")
 
 
 def _check(status: int, what: str) -> None:

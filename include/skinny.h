@@ -169,6 +169,31 @@ SK_API int sk_set_pdl(int enable);
  */
 SK_API void sk_inject_wait_timeout(int enable);
 
+/*
+ * nvfp4_gemm for callers that cannot allocate device memory (the pages have no
+ * counterpart; this is a library service).  nvfp4_gemm needs the workspace
+ * that sk_init() gets with cudaMalloc; code that must not allocate (inside an
+ * arena or pool allocator that owns all device memory, behind an allocator
+ * frozen after start-up, on a serving path with a no-allocation rule) calls
+ * this instead.  Its scratch memory is a fixed 8 MiB static device array,
+ * created when the library is loaded and held by every GPU that loads it until
+ * the process exits; the call itself allocates nothing (no cudaMalloc or
+ * cudaFree, no library allocation) and needs no sk_init().
+ *   Arguments, layouts and results are those of nvfp4_gemm (FP32 output).
+ *   SK_ERR_WORKSPACE: the split-K partial sums of this shape do not fit the
+ *   array (with K > 1024 they need ceil(N/16) * ceil(K/1024) * 64 * m bytes,
+ *   m = 1, 2, 4 or 8 for M = 1, 2, 3..4, 5..8, at most about 7 MiB).
+ *   The first call on a device (with that device current) looks up the
+ *   array's device address (cudaGetSymbolAddress), the tensor-map encoder and
+ *   the SM count: make it before any stream capture.  All calls share the one
+ *   array and leave their partial sums in it; each call clears the counters it
+ *   needs before its kernel runs.  Calls whose kernels overlap on the GPU
+ *   (different streams or host threads) race on the array.  Bounded-wait
+ *   timeouts of this entry point are not reported by sk_last_device_error().
+ */
+SK_API sk_status nvfp4_gemm_noalloc(const void *x, const uint8_t *W_codes, const uint8_t *W_scales,
+                                    float W_gscale, float *y, int M, int N, int K, void *stream);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 SK_API int sk_version(void);
 
