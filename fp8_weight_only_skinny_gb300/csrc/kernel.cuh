@@ -446,7 +446,7 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
     if (threadIdx.x == 0) {
         for (int s = 0; s < T::STAGES; ++s) {
             mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, 4);
+            mbar_init(bar_empty + 8 * s, 1);
         }
         flags[0] = 0;
         fence_barrier_init();
@@ -515,22 +515,26 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
         if constexpr (MP == 8) {
             float d[4];
             unit_mma<FMT>(d, xr, stage, p, g, c, w, lane);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty + 8 * s);
             const int r = lane >> 2, qq = lane & 3;
             *reinterpret_cast<float2 *>(gred + w * 128 + r * 8 + 2 * qq) = make_float2(d[0], d[1]);
             *reinterpret_cast<float2 *>(gred + w * 128 + (r + 8) * 8 + 2 * qq) = make_float2(d[2], d[3]);
         } else {
             float out[4 * MP];
             unit_simt<FMT, MP>(out, xr, stage, p, g, c, w, lane);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty + 8 * s);
             warp_reduce_split<4 * MP>(out, lane);
             constexpr int NV = 4 * MP;
             const int idx = reduce_index<NV>(lane);    // lanes holding a distinct value
             if ((lane & ((32 / NV) - 1)) == 0) gred[(4 * w) * MP + idx] = out[0];
         }
         named_bar_sync(bar_id, GROUP_THREADS);
+        // Release the stage only now.  The MMAs / FMAs that consume the shared
+        // loads touch registers only, so an arrive placed right after them in
+        // program order may be performed before the last loads of the tile
+        // have read it, and the producer's next copy into the stage could
+        // then overwrite words not yet read.  The reduction-buffer stores
+        // depend on every loaded word, and the group barrier orders them (and
+        // so the loads) before this arrive.
+        if (t == 0) mbar_arrive(bar_empty + 8 * s);
 
         // output t of this unit: row t / MP, token t % MP
         if (t < NOUT) {
@@ -550,18 +554,22 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
         // CTAs that complete nothing leave at once.
         int *fix_n = const_cast<int *>(flags) + 2;
         int *fix_list = const_cast<int *>(flags) + 16;          // CT entries
-        __threadfence();                               // release this thread's partials
         for (int b0 = 0; b0 < n_units; b0 += CT) {
             if (ct == 0) *fix_n = 0;
             named_bar_sync(15, CT);
+            // Release: the barrier orders every thread's partial stores before
+            // this fence, and the fence orders them before this thread's atomic.
+            // Acquire: the same fence after the atomic, before the barrier that
+            // precedes every thread's partial loads.
             const int i = b0 + ct;
             if (i < n_units) {
                 const int g = int((u_lo + i) % p.G);
+                __threadfence();
                 if (atomicAdd(counters + g, 1u) == unsigned(p.C - 1)) fix_list[atomicAdd(fix_n, 1)] = g;
+                __threadfence();
             }
             named_bar_sync(15, CT);
             const int n_fix = *fix_n;
-            __threadfence();                           // acquire the other CTAs' partials
             constexpr int ES = CT / NOUT;
             const int o = ct % NOUT;
             for (int e = ct / NOUT; e < n_fix; e += 4 * ES) {
@@ -589,13 +597,15 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
 
     if (MP == 8 && p.C > 1) {
         // Split-K fix-up, MMA variant (128 outputs per row group: the sums are
-        // the heavy part, so they are shared out evenly).  (1) Publish: every thread releases its partial stores,
-        // then one fire-and-forget counter increment per unit of this CTA.
-        // (2) Finish: row group g belongs to CTA g mod P (an even share for
-        // every CTA); it waits (bounded) until all C partials of each of its
-        // row groups are published and sums them in ascending chunk order.
-        __threadfence();
+        // the heavy part, so they are shared out evenly).  (1) Publish: after a
+        // CTA barrier (which orders every thread's partial stores before it),
+        // each thread fences and then makes fire-and-forget counter increments,
+        // one per unit of this CTA: fence and atomic by the same thread form
+        // the release.  (2) Finish: row group g belongs to CTA g mod P (an even
+        // share for every CTA); it waits (bounded) until all C partials of each
+        // of its row groups are published and sums them in ascending chunk order.
         named_bar_sync(15, CT);
+        __threadfence();
         for (int i = ct; i < n_units; i += CT) atomicAdd(counters + int((u_lo + i) % p.G), 1u);
         const int P = gridDim.x;
         const int n_own = p.G > int(blockIdx.x) ? (p.G - 1 - int(blockIdx.x)) / P + 1 : 0;
@@ -613,8 +623,9 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
                 if (flags[0]) break;
             }
         }
+        // Thread 0's acquire loads precede this barrier, which orders them
+        // before every thread's partial loads.
         named_bar_sync(15, CT);
-        __threadfence();                               // acquire the published partials
         // Thread ct sums output o of owned row groups e0, e0 + ES, ...; four
         // row groups at a time so that their loads are in flight together.
         constexpr int ES = CT / NOUT;
@@ -650,10 +661,10 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
             unsigned long long k = 0;
             for (int e = ct; e < CT; e += MP) k = keys[e] > k ? keys[e] : k;
             if (k != 0 && ct < p.M) atomicMax(&ctrl->argmax_key[ct], k);
-            __threadfence();
         }
         named_bar_sync(15, CT);
         if (ct == 0) {
+            __threadfence();                   // release the key updates ordered by the barrier
             const unsigned int old = atomicAdd(&ctrl->done, 1u);
             if (old == gridDim.x - 1) {
                 __threadfence();
