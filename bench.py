@@ -301,6 +301,24 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def aggregate(ms_local, bytes_per_rank, dist=None):
+    """Whole-job throughput over all ranks: every rank processes bytes_per_rank
+    per step (replicas, weak scaling); the step time is the slowest rank's.
+    Returns (GB/s, max ms)."""
+    import torch
+
+    ms = float(ms_local)
+    world = 1
+    if dist is not None and dist.is_initialized():
+        world = dist.get_world_size()
+        t = torch.tensor([ms], dtype=torch.float64)
+        if dist.get_backend() == "nccl":
+            t = t.cuda()
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return world * bytes_per_rank / (ms * 1e-3) / 1e9, ms
+
+
 def config(M):
     return {"workload": f"decode round: {N_LAYERS} x (qkv FP8 5120x7168, o_proj FP8 6144x5120, "
                         f"gate_up NVFP4 5120x34816, down NVFP4 17408x5120) + NVFP4 lm_head 5120x151936 "
@@ -369,12 +387,7 @@ def run_ours(args):
             torch.cuda.synchronize()
             if barrier:
                 barrier()
-    ms = e0.elapsed_time(e1) / args.steps
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * STEP_BYTES / (ms * 1e-3) / 1e9
+    value, ms = aggregate(e0.elapsed_time(e1) / args.steps, STEP_BYTES, dist)
     st = sk.last_device_error(stream)
     if st != 0:
         raise RuntimeError(f"device error {st}")
@@ -396,11 +409,8 @@ def run_ours(args):
         am_host.copy_(head.am, non_blocking=True)
 
     g2 = capture(e2e_step, stream)
-    e2e_ms = time_graph(g2, stream, reps=args.steps, warmup=3, barrier=barrier)
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_value, e2e_ms = aggregate(time_graph(g2, stream, reps=args.steps, warmup=3, barrier=barrier),
+                                  STEP_BYTES, dist)
     del g2
 
     # ---- dominant kernel alone (NVFP4 gate_up launch at this M), cold L2
@@ -435,7 +445,7 @@ def run_ours(args):
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs)" if peak_kind == "measured"
                          else "fallback 6.8 TB/s"},
-            "e2e": {"value": round(world * STEP_BYTES / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
                     "h2d_bytes_per_step": int(x_dev.numel() * 2), "d2h_bytes_per_step": int(M * 4),
                     "ms_per_step": round(e2e_ms, 4)},
             "gpu_launches": launches_per_step * args.steps,

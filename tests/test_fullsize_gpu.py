@@ -1,0 +1,152 @@
+"""Parity at the full decode-layer sizes, in the launch configuration the
+benchmark uses (default grid, PDL on), on sampled output columns the oracle
+computes one by one; and a CUDA-graph-replayed decode stack (the benchmark's
+step structure, shortened) checked the same way."""
+import functools
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import check, dev, host
+
+
+@functools.lru_cache(maxsize=None)
+def _nv(N, K, seed):
+    return synth.nvfp4_weights(N, K, seed=seed)
+
+
+@functools.lru_cache(maxsize=None)
+def _f8(N, K, seed):
+    return synth.fp8_weights(N, K, seed=seed)
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [("qkv", 5120, 7168), ("o_proj", 6144, 5120), ("gate_up", 5120, 34816), ("down", 17408, 5120)]
+
+
+@pytest.fixture(scope="module")
+def sk():
+    import torch
+
+    torch.cuda.set_device(0)
+    import fp8_weight_only_skinny_gb300 as skm
+
+    skm.init()
+    yield skm
+    assert skm.last_device_error() == skm.SK_OK
+
+
+def _cols(N, n=192, seed=0):
+    r = np.random.default_rng(seed)
+    # the first and last row groups, chunk-boundary rows and random ones
+    fixed = [0, 1, 15, 16, N // 2, N - 17, N - 16, N - 1]
+    return np.unique(np.concatenate([fixed, r.choice(N, n, replace=False)]))
+
+
+@pytest.mark.parametrize("name,K,N", SHAPES)
+@pytest.mark.parametrize("M", [1, 8])
+def test_nvfp4_full_size_sampled(sk, name, K, N, M):
+    x = synth.x_f16(M, K, seed=K + M)
+    codes, scales, g = _nv(N, K, N)
+    y = host(sk.nvfp4_gemm(dev(x), dev(codes), dev(scales), float(g)))
+    cols = _cols(N, seed=N + M)
+    y_ref, l1 = oracle.nvfp4_linear(x, codes, scales, g, cols=cols)
+    check(y[:, cols], y_ref, l1, False, f"nvfp4 {name} M={M}")
+
+
+@pytest.mark.parametrize("name,K,N", SHAPES)
+@pytest.mark.parametrize("M", [1, 8])
+def test_fp8_full_size_sampled(sk, name, K, N, M):
+    x = synth.x_f16(M, K, seed=K + M + 1)
+    codes, scales = _f8(N, K, N + 1)
+    y = host(sk.fp8_gemm(dev(x), dev(codes), dev(scales), f16_out=True))
+    cols = _cols(N, seed=N + M + 1)
+    y_ref, l1 = oracle.fp8_linear(x, codes, scales, cols=cols)
+    check(y[:, cols], y_ref, l1, True, f"fp8 {name} M={M}")
+
+
+@pytest.mark.parametrize("M", [1, 8])
+def test_lm_head_full_size(sk, M):
+    K, N = synth.LM_HEAD_SHAPE
+    x = synth.x_f16(M, K, seed=100 + M)
+    codes, scales, g = _nv(N, K, 101)
+    logits, am = sk.lm_head_argmax(dev(x), dev(codes), dev(scales), float(g))
+    lg, am = host(logits), host(am)
+    for m in range(M):                       # the fused pick is the argmax of the same logits
+        assert am[m] == int(np.argmax(lg[m]))
+    cols = np.unique(np.concatenate([_cols(N, 256, seed=M), am.astype(np.int64)]))
+    y_ref, l1 = oracle.nvfp4_linear(x, codes, scales, g, cols=cols)
+    check(lg[:, cols], y_ref, l1, False, f"lm_head M={M}")
+    # the picked logit is, within tolerance, at least every sampled logit
+    tol = oracle.tolerance(l1)
+    for m in range(M):
+        j = int(np.where(cols == am[m])[0][0])
+        assert np.all(y_ref[m, j] + tol[m, j] + tol[m] >= y_ref[m])
+
+
+@pytest.mark.parametrize("M", [1, 8])
+def test_graph_replayed_stack(sk, M):
+    """Two decoder layers (qkv/o FP8, gate_up/down NVFP4) and the lm_head,
+    captured once into a CUDA graph with PDL between the calls and replayed
+    three times: every output equals the eager result bitwise and the oracle on
+    sampled columns."""
+    import torch
+
+    layers = []
+    for li in range(2):
+        for name, K, N in SHAPES:
+            fmt = "fp8" if name in ("qkv", "o_proj") else "nvfp4"
+            x = synth.x_f16(M, K, seed=1000 * li + K)
+            if fmt == "fp8":
+                w = synth.fp8_weights(N, K, seed=2000 * li + N)
+            else:
+                w = synth.nvfp4_weights(N, K, seed=2000 * li + N)
+            layers.append((name, fmt, x, w, tuple(dev(a) for a in (x, *w[:2])),
+                           torch.empty((M, N), dtype=torch.float16, device="cuda:0")))
+    K, N = synth.LM_HEAD_SHAPE
+    hx = synth.x_f16(M, K, seed=7)
+    hw = synth.nvfp4_weights(N, K, seed=8)
+    hd = (dev(hx), dev(hw[0]), dev(hw[1]))
+    logits = torch.empty((M, N), dtype=torch.float32, device="cuda:0")
+    am = torch.empty((M,), dtype=torch.int32, device="cuda:0")
+
+    def step():
+        for name, fmt, x, w, d, y in layers:
+            if fmt == "fp8":
+                sk.fp8_gemm(d[0], d[1], d[2], y=y, f16_out=True)
+            else:
+                sk.nvfp4_gemm(d[0], d[1], d[2], float(w[2]), y=y, f16_out=True)
+        sk.lm_head_argmax(hd[0], hd[1], hd[2], float(hw[2]), logits=logits, argmax=am)
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        step()
+    s.synchronize()
+    eager = [host(l[5]) for l in layers] + [host(logits), host(am)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step()
+    for _ in range(3):
+        with torch.cuda.stream(s):                 # poison and replay on the same stream
+            for l in layers:
+                l[5].fill_(float("nan"))
+            logits.fill_(float("nan"))
+            g.replay()
+        s.synchronize()
+        got = [host(l[5]) for l in layers] + [host(logits), host(am)]
+        for idx, (a, b) in enumerate(zip(got, eager)):
+            assert np.array_equal(a, b), (idx, int(np.sum(~(a == b))), a.size)
+    for (name, fmt, x, w, d, y), yv in zip(layers, eager):
+        Nl = w[0].shape[0]
+        cols = _cols(Nl, 64, seed=Nl)
+        if fmt == "fp8":
+            y_ref, l1 = oracle.fp8_linear(x, w[0], w[1], cols=cols)
+        else:
+            y_ref, l1 = oracle.nvfp4_linear(x, w[0], w[1], w[2], cols=cols)
+        check(yv[:, cols], y_ref, l1, True, f"stack {name}")
+    cols = _cols(N, 64, seed=3)
+    y_ref, l1 = oracle.nvfp4_linear(hx, hw[0], hw[1], hw[2], cols=cols)
+    check(eager[-2][:, cols], y_ref, l1, False, "stack lm_head")
