@@ -599,36 +599,42 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
         // Split-K fix-up, MMA variant (128 outputs per row group: the sums are
         // the heavy part, so they are shared out evenly).  (1) Publish: after a
         // CTA barrier (which orders every thread's partial stores before it),
-        // each thread fences and then makes fire-and-forget counter increments,
-        // one per unit of this CTA: fence and atomic by the same thread form
-        // the release.  (2) Finish: row group g belongs to CTA g mod P (an even
-        // share for every CTA); it waits (bounded) until all C partials of each
-        // of its row groups are published and sums them in ascending chunk order.
+        // each thread that has units to publish fences and then makes
+        // fire-and-forget counter increments, one per unit of this CTA: fence
+        // and atomic by the same thread form the release.  (2) Finish: row
+        // group g belongs to CTA g mod P (an even share for every CTA).  Its
+        // counters are polled in parallel, one thread per owned row group
+        // (bounded), and then each output sums its C partials in ascending
+        // chunk order.
         named_bar_sync(15, CT);
-        __threadfence();
-        for (int i = ct; i < n_units; i += CT) atomicAdd(counters + int((u_lo + i) % p.G), 1u);
+        if (ct < n_units) {
+            __threadfence();
+            for (int i = ct; i < n_units; i += CT) atomicAdd(counters + int((u_lo + i) % p.G), 1u);
+        }
         const int P = gridDim.x;
         const int n_own = p.G > int(blockIdx.x) ? (p.G - 1 - int(blockIdx.x)) / P + 1 : 0;
-        if (ct == 0) {
+        for (int e = ct; e < n_own; e += CT) {
+            const unsigned int *cnt = counters + int(blockIdx.x) + e * P;
+            if (ld_acquire_u32(cnt) == unsigned(p.C)) continue;
             const uint64_t t0 = globaltimer_ns();
-            for (int e = 0; e < n_own; ++e) {
-                const unsigned int *cnt = counters + int(blockIdx.x) + e * P;
-                while (ld_acquire_u32(cnt) != unsigned(p.C)) {
-                    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
-                        flags[0] = 1;
-                        atomicOr(&ctrl->err, ERR_TIMEOUT);
-                        break;
-                    }
+            for (;;) {
+                __nanosleep(32);
+                if (ld_acquire_u32(cnt) == unsigned(p.C) || flags[0]) break;
+                if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+                    flags[0] = 1;
+                    atomicOr(&ctrl->err, ERR_TIMEOUT);
+                    break;
                 }
-                if (flags[0]) break;
             }
         }
-        // Thread 0's acquire loads precede this barrier, which orders them
-        // before every thread's partial loads.
+        // The polling threads' acquire loads precede this barrier, which
+        // orders them before every thread's partial loads.
         named_bar_sync(15, CT);
-        // Thread ct sums output o of owned row groups e0, e0 + ES, ...; four
-        // row groups at a time so that their loads are in flight together.
+        // Thread ct sums output o of owned row groups e0, e0 + ES, ... (up to
+        // four at a time), loading eight chunks of each before adding them so
+        // that up to 32 loads are in flight per thread.
         constexpr int ES = CT / NOUT;
+        constexpr int CB = 8;
         const int o = ct % NOUT;
         for (int e = ct / NOUT; e < n_own; e += 4 * ES) {
             int gg[4];
@@ -638,11 +644,20 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
                 gg[j] = e + j * ES < n_own ? int(blockIdx.x) + (e + j * ES) * P : -1;
                 acc[j] = 0.f;
             }
-#pragma unroll 4
-            for (int cc = 0; cc < p.C; ++cc) {
+            for (int c0 = 0; c0 < p.C; c0 += CB) {
+                float v[4][CB];
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    if (gg[j] >= 0) acc[j] += ld_cg_f32(partials + ((size_t)gg[j] * p.C + cc) * NOUT + o);
+#pragma unroll
+                    for (int k = 0; k < CB; ++k)
+                        v[j][k] = (gg[j] >= 0 && c0 + k < p.C)
+                                      ? ld_cg_f32(partials + ((size_t)gg[j] * p.C + c0 + k) * NOUT + o)
+                                      : 0.f;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                    for (int k = 0; k < CB; ++k)
+                        if (c0 + k < p.C) acc[j] += v[j][k];
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j)
