@@ -9,6 +9,9 @@ from ._binding import (  # noqa: F401
     LIB_PATH,
     SK_OK,
     STATUS,
+    VARIANT_AUTO,
+    VARIANT_SIMT,
+    VARIANT_TENSOR,
     SkinnyError,
     fp8_gemm,
     init,
@@ -17,6 +20,7 @@ from ._binding import (  # noqa: F401
     lm_head_argmax,
     nvfp4_gemm,
     set_pdl,
+    set_variant,
     shutdown,
     status_string,
 )

@@ -48,6 +48,7 @@ def _load() -> ctypes.CDLL:
         "sk_status_string": ([i], ctypes.c_char_p),
         "sk_last_device_error": ([p], i),
         "sk_set_pdl": ([i], i),
+        "sk_set_variant": ([i], i),
         "sk_version": ([], i),
         "sk_inject_wait_timeout": ([i], None),
         "nvfp4_gemm_noalloc": ([p, p, p, f, p, i, i, i, p], i),
@@ -64,7 +65,7 @@ lib = _load()
 # Names declared in include/skinny.h (the tests check that each is exported).
 EXPORTS = ("sk_init", "sk_shutdown", "nvfp4_gemm", "nvfp4_gemm_f16out", "fp8_gemm",
            "fp8_gemm_f16out", "lm_head_argmax", "sk_status_string", "sk_last_device_error",
-           "sk_set_pdl", "sk_inject_wait_timeout", "nvfp4_gemm_noalloc", "sk_version")
+           "sk_set_pdl", "sk_set_variant", "sk_inject_wait_timeout", "nvfp4_gemm_noalloc", "sk_version")
 
 
 def _check(status: int, what: str) -> None:
@@ -87,6 +88,17 @@ def shutdown() -> None:
 
 def set_pdl(enable: bool) -> bool:
     return bool(lib.sk_set_pdl(1 if enable else 0))
+
+
+VARIANT_AUTO, VARIANT_TENSOR, VARIANT_SIMT = 0, 1, 2
+
+
+def set_variant(variant: int) -> int:
+    """Kernel variant (VARIANT_AUTO, VARIANT_TENSOR or VARIANT_SIMT); returns the previous one."""
+    prev = int(lib.sk_set_variant(int(variant)))
+    if prev < 0:
+        raise ValueError(f"unknown kernel variant {variant}")
+    return prev
 
 
 def _stream_ptr(stream):

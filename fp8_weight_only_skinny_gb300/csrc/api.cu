@@ -29,6 +29,7 @@ DeviceState g_dev[MAX_DEVICES];
 std::mutex g_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 int g_pdl = 1;
+std::atomic<int> g_variant{SK_VARIANT_AUTO};
 std::atomic<int> g_inject_stall{0};
 
 sk_status resolve_encode() {
@@ -65,17 +66,6 @@ DeviceState *current(int *dev_out) {
     if (dev_out) *dev_out = dev;
     DeviceState *d = &g_dev[dev];
     return d->ws ? d : nullptr;
-}
-
-// Token count padded to the kernel variant: 1, 2, 4 (SIMT) or 8 (MMA).
-// SK_FORCE_VARIANT=mma makes every M use the MMA variant (for A/B tests).
-int padded_m(int M) {
-    const char *f = std::getenv("SK_FORCE_VARIANT");
-    if (f && std::strcmp(f, "mma") == 0) return 8;
-    if (M <= 1) return 1;
-    if (M == 2) return 2;
-    if (M <= 4) return 4;
-    return 8;
 }
 
 // Persistent grid: CTAS_PER_SM CTAs per SM, never more CTAs than units.
@@ -126,7 +116,6 @@ sk_status run(Kind kind, const void *x, const uint8_t *codes, const void *scales
     if (N == 0) return SK_OK;
     if (K == 0) return zero_outputs(y, size_t(M) * N * (f16 ? 2 : 4), argmax, M, s);
 
-    const int mp = padded_m(M);
     sk::Params p = {};
     p.x = reinterpret_cast<const __half *>(x);
     p.fp8_scales = nv ? nullptr : reinterpret_cast<const float *>(scales);
@@ -141,12 +130,13 @@ sk_status run(Kind kind, const void *x, const uint8_t *codes, const void *scales
     p.C = (K + sk::KC - 1) / sk::KC;
     p.KB = (K + 127) / 128;
     p.U = (long long)p.G * p.C;
-    p.stall = g_inject_stall.exchange(0);
+    const int grid = grid_for(d, p.U);
+    const int mp = sk::choose_mp(M, nv, p.U, grid);
     if (p.C > 1) {
         const size_t need = size_t(p.U) * sk::unit_partial_bytes(mp);
         if (sk::WS_PARTIAL_OFFSET + need > d->bytes) return SK_ERR_WORKSPACE;
     }
-    const int grid = grid_for(d, p.U);
+    p.stall = g_inject_stall.exchange(0);
 
     CUtensorMap tm_codes, tm_scales;
     if (nv) {
@@ -164,6 +154,23 @@ sk_status run(Kind kind, const void *x, const uint8_t *codes, const void *scales
 }
 
 }  // namespace
+
+namespace sk {
+
+// Measured on GB300 (cold L2, graphs of back-to-back launches): for M >= 2 the
+// tensor-core variant is faster on every decode-layer shape (up to 2x at M = 4);
+// for M = 1 the SIMT variant wins only when each CTA streams many units (FP8
+// gate_up 5120x34816 at 36 units per CTA, NVFP4 lm_head at 156), because its
+// per-unit arithmetic is lighter while its fix-up and start-up are not.
+int choose_mp(int M, bool nvfp4, long long U, long long P) {
+    const int v = g_variant.load(std::memory_order_relaxed);
+    if (M > 1 || v == SK_VARIANT_TENSOR) return 8;
+    if (v == SK_VARIANT_SIMT) return 1;
+    const long long per_cta = U / (P > 0 ? P : 1);
+    return per_cta >= (nvfp4 ? 96 : 24) ? 1 : 8;
+}
+
+}  // namespace sk
 
 extern "C" {
 
@@ -262,6 +269,11 @@ sk_status sk_last_device_error(void *stream) {
         return SK_ERR_TIMEOUT;
     }
     return SK_OK;
+}
+
+int sk_set_variant(int variant) {
+    if (variant != SK_VARIANT_AUTO && variant != SK_VARIANT_TENSOR && variant != SK_VARIANT_SIMT) return -1;
+    return g_variant.exchange(variant);
 }
 
 int sk_set_pdl(int enable) {

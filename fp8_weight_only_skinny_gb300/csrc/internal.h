@@ -7,8 +7,8 @@ namespace sk {
 
 struct Params;
 
-// Launch one kernel of the given format.  mp: padded token count
-// (1, 2, 4 = SIMT path; 8 = MMA path).
+// Launch one kernel of the given format.  mp: token slots of the variant
+// (1 = single-token SIMT variant; 8 = tensor-core variant).
 cudaError_t launch_nvfp4(int mp, bool f16out, bool argmax, const CUtensorMap &tm_codes,
                          const CUtensorMap &tm_scales, const Params &p, int grid,
                          cudaStream_t stream, bool pdl);
@@ -17,5 +17,9 @@ cudaError_t launch_fp8(int mp, bool f16out, const CUtensorMap &tm_codes, const P
 
 // Bytes of workspace-resident partial sums one unit writes (16 rows x mp tokens).
 inline size_t unit_partial_bytes(int mp) { return size_t(16) * mp * 4; }
+
+// Token slots of the kernel variant for an M-token call of U units on a grid
+// of P CTAs: 1 (SIMT) or 8 (tensor-core), by the process-wide variant setting.
+int choose_mp(int M, bool nvfp4, long long U, long long P);
 
 }  // namespace sk

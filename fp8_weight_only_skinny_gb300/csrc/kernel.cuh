@@ -4,13 +4,14 @@
 // memory with 2-D TMA into an mbarrier ring, and two consumer groups of four
 // warps decode them in registers and multiply-accumulate in FP32:
 //
-//   * M <= 4 ("SIMT" path): E2M1 / E4M3 pairs -> f16x2 with cvt.rn.f16x2.*,
-//     exact FP16 products accumulated in FP32 with the mixed-precision FMA,
-//     the 16-element (NVFP4) or 128x128 (FP8) block scale applied once per
-//     block sum.
-//   * M = 5..8 ("MMA" path, the 8-row speculative-verify round): swap-AB
-//     mma.sync.m16n8k16 with the 16 weight rows as the 16-wide operand and the
-//     (zero-padded) 8 tokens as the 8-wide one.  For NVFP4 each decoded pair
+//   * MP = 1 ("SIMT" variant, one token): E2M1 / E4M3 pairs -> f16x2 with
+//     cvt.rn.f16x2.*, exact FP16 products accumulated in FP32 with the
+//     mixed-precision FMA, the 16-element (NVFP4) or 128x128 (FP8) block scale
+//     applied once per block sum.  The template also compiles for MP = 2 and
+//     4, but the library instantiates MP = 1 only.
+//   * MP = 8 ("MMA" variant, M = 1..8 tokens; the 8-row speculative-verify
+//     round fills it): swap-AB mma.sync.m16n8k16 with the 16 weight rows as the
+//     16-wide operand and the (zero-padded) 8 tokens as the 8-wide one.  For NVFP4 each decoded pair
 //     is multiplied by its E4M3 block scale in FP16 first, which is exact
 //     (E2M1 has 2 and E4M3 4 significant bits, and their product stays in the
 //     FP16 normal range), so the MMA sees exact weights and accumulates in

@@ -37,12 +37,8 @@ cudaError_t launch_variant(const CUtensorMap &tm_codes, const CUtensorMap &tm_sc
 template <int FMT, bool F16OUT, bool ARGMAX>
 cudaError_t launch_by_m(int mp, const CUtensorMap &tm_codes, const CUtensorMap &tm_scales,
                         const Params &p, int grid, cudaStream_t stream, bool pdl) {
-    switch (mp) {
-        case 1: return launch_variant<FMT, 1, F16OUT, ARGMAX>(tm_codes, tm_scales, p, grid, stream, pdl);
-        case 2: return launch_variant<FMT, 2, F16OUT, ARGMAX>(tm_codes, tm_scales, p, grid, stream, pdl);
-        case 4: return launch_variant<FMT, 4, F16OUT, ARGMAX>(tm_codes, tm_scales, p, grid, stream, pdl);
-        default: return launch_variant<FMT, 8, F16OUT, ARGMAX>(tm_codes, tm_scales, p, grid, stream, pdl);
-    }
+    if (mp == 1) return launch_variant<FMT, 1, F16OUT, ARGMAX>(tm_codes, tm_scales, p, grid, stream, pdl);
+    return launch_variant<FMT, 8, F16OUT, ARGMAX>(tm_codes, tm_scales, p, grid, stream, pdl);
 }
 
 }  // namespace sk

@@ -102,13 +102,15 @@ sk_status nvfp4_gemm_noalloc(const void *x, const uint8_t *W_codes, const uint8_
     if (size_t(N) > sk::WS_MAX_ROWGROUPS * sk::RG) return SK_ERR_UNSUPPORTED_SHAPE;
     if (!na_aligned(x, 16) || !na_aligned(W_codes, 16) || !na_aligned(W_scales, 16)) return SK_ERR_MISALIGNED;
     if (!na_aligned(y, 4)) return SK_ERR_MISALIGNED;
-    const int mp = M <= 1 ? 1 : (M == 2 ? 2 : (M <= 4 ? 4 : 8));
+    NoAllocDevice *d = nullptr;
+    if (sk_status st = setup_current(&d); st != SK_OK) return st;
     const long long G = (N + sk::RG - 1) / sk::RG, C = (K + sk::KC - 1) / sk::KC;
+    const long long cap = (long long)(d->num_sms > 0 ? d->num_sms : 1) * 2;
+    const int grid = int(G * C < cap ? G * C : cap);
+    const int mp = sk::choose_mp(M, true, G * C, grid);
     // The split-K partial sums must fit in the static scratch.
     if (C > 1 && sk::WS_PARTIAL_OFFSET + size_t(G * C) * sk::unit_partial_bytes(mp) > NOALLOC_SCRATCH_BYTES)
         return SK_ERR_WORKSPACE;
-    NoAllocDevice *d = nullptr;
-    if (sk_status st = setup_current(&d); st != SK_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (N == 0) return SK_OK;
     if (K == 0) return cudaMemsetAsync(y, 0, size_t(M) * N * 4, s) == cudaSuccess ? SK_OK : SK_ERR_CUDA;
@@ -135,8 +137,6 @@ sk_status nvfp4_gemm_noalloc(const void *x, const uint8_t *W_codes, const uint8_
     p.KB = (K + 127) / 128;
     p.U = G * C;
     p.stall = 0;
-    const long long cap = (long long)(d->num_sms > 0 ? d->num_sms : 1) * 2;
-    const int grid = int(p.U < cap ? p.U : cap);
     CUtensorMap tm_codes, tm_scales;
     if (!na_encode_map(&tm_codes, W_codes, uint64_t(K) / 2, uint64_t(N), sk::Traits<sk::NVFP4>::CODE_BOX_X) ||
         !na_encode_map(&tm_scales, W_scales, uint64_t(K) / 16, uint64_t(N), sk::Traits<sk::NVFP4>::SCALE_BOX_X))

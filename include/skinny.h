@@ -160,6 +160,22 @@ SK_API sk_status sk_last_device_error(void *stream);
 SK_API int sk_set_pdl(int enable);
 
 /*
+ * Kernel variant, process-wide; returns the previous setting, or -1 (and
+ * changes nothing) for a value outside the three below.
+ *   SK_VARIANT_AUTO (default): the tensor-core variant (swap-AB m16n8k16 MMA,
+ *     tokens padded to 8) for every M, except M = 1 on shapes with many work
+ *     units (16 rows x 1024 k) per CTA -- at least 24 for FP8, 96 for NVFP4 --
+ *     where the single-token SIMT variant (mixed FP16 x FP16 + FP32 FMA) is
+ *     faster.  Both thresholds are measured on GB300.
+ *   SK_VARIANT_TENSOR: the tensor-core variant for every M.
+ *   SK_VARIANT_SIMT: the SIMT variant for M = 1 (tensor-core for M > 1).
+ * Both variants meet the same accuracy bound; each is bitwise reproducible,
+ * but they sum in different orders, so their results differ in the last bits.
+ */
+enum { SK_VARIANT_AUTO = 0, SK_VARIANT_TENSOR = 1, SK_VARIANT_SIMT = 2 };
+SK_API int sk_set_variant(int variant);
+
+/*
  * Failure-injection hook for tests: with enable = 1 the next kernel launched
  * by this process on any device issues no weight copies, so its consumers'
  * bounded waits run out (about one second); the kernel then finishes without

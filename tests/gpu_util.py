@@ -1,4 +1,6 @@
 """Helpers shared by the GPU tests: device placement and oracle comparison."""
+import contextlib
+
 import numpy as np
 
 import oracle
@@ -8,6 +10,17 @@ def dev(a):
     import torch
 
     return torch.from_numpy(np.ascontiguousarray(a)).to("cuda:0")
+
+
+@contextlib.contextmanager
+def variant(sk, name):
+    """Run the block with the kernel variant `name` ("auto", "tensor" or "simt")."""
+    code = {"auto": sk.VARIANT_AUTO, "tensor": sk.VARIANT_TENSOR, "simt": sk.VARIANT_SIMT}[name]
+    prev = sk.set_variant(code)
+    try:
+        yield
+    finally:
+        sk.set_variant(prev)
 
 
 def host(t):

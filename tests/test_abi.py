@@ -98,3 +98,16 @@ def test_misaligned_pointers_rejected():
     assert _f8(c=A + 8) == MISALIGNED
     assert _lm(am=A + 2) == MISALIGNED
     assert _lm(lg=A + 2) == MISALIGNED
+
+
+def test_variant_setting_round_trips_and_rejects_unknown_values():
+    prev = sk.set_variant(sk.VARIANT_TENSOR)
+    try:
+        assert sk.set_variant(sk.VARIANT_SIMT) == sk.VARIANT_TENSOR
+        assert sk.lib.sk_set_variant(3) == -1          # unknown: nothing changes
+        assert sk.lib.sk_set_variant(-1) == -1
+        with pytest.raises(ValueError):
+            sk.set_variant(7)
+        assert sk.set_variant(sk.VARIANT_AUTO) == sk.VARIANT_SIMT
+    finally:
+        sk.set_variant(prev)

@@ -9,7 +9,7 @@ import pytest
 
 import oracle
 import synth
-from gpu_util import check, dev, host
+from gpu_util import check, dev, host, variant
 
 pytestmark = pytest.mark.gpu
 
@@ -33,33 +33,39 @@ def max_ctas(request):
     del os.environ["SK_MAX_CTAS"]
 
 
-@pytest.mark.parametrize("M", [1, 2, 4, 8])
+MV = [(1, "simt"), (1, "tensor"), (2, "auto"), (4, "auto"), (8, "auto")]
+
+
+@pytest.mark.parametrize("M,var", MV)
 @pytest.mark.parametrize("K,N", [(1024, 520), (3072, 200), (5120, 96)])
-def test_nvfp4_many_units_per_cta(sk, max_ctas, M, K, N):
+def test_nvfp4_many_units_per_cta(sk, max_ctas, M, var, K, N):
     x = synth.x_f16(M, K, seed=K + M)
     codes, scales, g = synth.nvfp4_weights(N, K, seed=N + 1)
     y_ref, l1 = oracle.nvfp4_linear(x, codes, scales, g)
-    y = host(sk.nvfp4_gemm(dev(x), dev(codes), dev(scales), float(g)))
+    with variant(sk, var):
+        y = host(sk.nvfp4_gemm(dev(x), dev(codes), dev(scales), float(g)))
     check(y, y_ref, l1, False, f"nvfp4 ctas={max_ctas} M{M} K{K} N{N}")
 
 
-@pytest.mark.parametrize("M", [1, 2, 4, 8])
+@pytest.mark.parametrize("M,var", MV)
 @pytest.mark.parametrize("K,N", [(1024, 520), (3072, 200), (4096, 130)])
-def test_fp8_many_units_per_cta(sk, max_ctas, M, K, N):
+def test_fp8_many_units_per_cta(sk, max_ctas, M, var, K, N):
     x = synth.x_f16(M, K, seed=K + M + 5)
     codes, scales = synth.fp8_weights(N, K, seed=N + 2)
     y_ref, l1 = oracle.fp8_linear(x, codes, scales)
-    y = host(sk.fp8_gemm(dev(x), dev(codes), dev(scales), f16_out=True))
+    with variant(sk, var):
+        y = host(sk.fp8_gemm(dev(x), dev(codes), dev(scales), f16_out=True))
     check(y, y_ref, l1, True, f"fp8 ctas={max_ctas} M{M} K{K} N{N}")
 
 
-@pytest.mark.parametrize("M", [1, 8])
-def test_lm_head_many_units_per_cta(sk, max_ctas, M):
+@pytest.mark.parametrize("M,var", [(1, "simt"), (1, "tensor"), (8, "auto")])
+def test_lm_head_many_units_per_cta(sk, max_ctas, M, var):
     K, N = 2048, 1000
     x = synth.x_f16(M, K, seed=77 + M)
     codes, scales, g = synth.nvfp4_weights(N, K, seed=78)
     y_ref, l1 = oracle.nvfp4_linear(x, codes, scales, g)
-    logits, am = sk.lm_head_argmax(dev(x), dev(codes), dev(scales), float(g))
+    with variant(sk, var):
+        logits, am = sk.lm_head_argmax(dev(x), dev(codes), dev(scales), float(g))
     lg = host(logits)
     check(lg, y_ref, l1, False, "lm_head few CTAs")
     am = host(am)

@@ -5,14 +5,12 @@ inputs and compares with the oracle under the accuracy contract
 |y - y_ref| <= 1e-3 * sum|x*w| + 1e-6 (+ one FP16 ulp for FP16 output).
 Exact cases (identity, one-hot, single-product decodes) are compared bitwise.
 """
-import os
-
 import numpy as np
 import pytest
 
 import oracle
 import synth
-from gpu_util import check, dev, host
+from gpu_util import check, dev, host, variant
 
 pytestmark = pytest.mark.gpu
 
@@ -65,6 +63,30 @@ def test_nvfp4_ragged_shapes(sk, K, N, M):
 F8_SHAPES = [(128, 1), (384, 17), (1024, 128), (1152, 129), (2048, 300), (3200, 40)]
 
 
+@pytest.mark.parametrize("K,N", NV_SHAPES)
+@pytest.mark.parametrize("var", ["simt", "tensor"])
+def test_nvfp4_ragged_shapes_one_token_variants(sk, K, N, var):
+    """M = 1 through each kernel variant explicitly (the automatic choice
+    depends on the shape)."""
+    x = synth.x_f16(1, K, seed=K + N + 11)
+    codes, scales, g = synth.nvfp4_weights(N, K, seed=K * 7 + N)
+    y_ref, l1 = oracle.nvfp4_linear(x, codes, scales, g)
+    with variant(sk, var):
+        check(nv_run(sk, x, codes, scales, g), y_ref, l1, False, f"nvfp4 {var} K{K} N{N}")
+        check(nv_run(sk, x, codes, scales, g, True), y_ref, l1, True, f"nvfp4 f16 {var} K{K} N{N}")
+
+
+@pytest.mark.parametrize("K,N", F8_SHAPES)
+@pytest.mark.parametrize("var", ["simt", "tensor"])
+def test_fp8_ragged_shapes_one_token_variants(sk, K, N, var):
+    x = synth.x_f16(1, K, seed=K + N + 12)
+    codes, scales = synth.fp8_weights(N, K, seed=K * 5 + N)
+    y_ref, l1 = oracle.fp8_linear(x, codes, scales)
+    with variant(sk, var):
+        check(f8_run(sk, x, codes, scales), y_ref, l1, False, f"fp8 {var} K{K} N{N}")
+        check(f8_run(sk, x, codes, scales, True), y_ref, l1, True, f"fp8 f16 {var} K{K} N{N}")
+
+
 @pytest.mark.parametrize("K,N", F8_SHAPES)
 @pytest.mark.parametrize("M", [1, 2, 4, 6, 8])
 def test_fp8_ragged_shapes(sk, K, N, M):
@@ -75,23 +97,32 @@ def test_fp8_ragged_shapes(sk, K, N, M):
     check(f8_run(sk, x, codes, scales, True), y_ref, l1, True, f"fp8 f16 M{M} K{K} N{N}")
 
 
-@pytest.mark.parametrize("M", [1, 8])
-def test_long_k_many_partials(sk, M):
+ONE_AND_EIGHT = [(1, "simt"), (1, "tensor"), (8, "auto")]
+
+
+@pytest.mark.parametrize("M,var", ONE_AND_EIGHT)
+def test_long_k_many_partials(sk, M, var):
     """K = 17408 gives 17 k-chunks per row group: the split-K fix-up path."""
     K, N = 17408, 48
     x = synth.x_f16(M, K, seed=21)
     codes, scales, g = synth.nvfp4_weights(N, K, seed=21)
     y_ref, l1 = oracle.nvfp4_linear(x, codes, scales, g)
-    check(nv_run(sk, x, codes, scales, g), y_ref, l1, False, "nvfp4 long K")
     c8, s8 = synth.fp8_weights(N, K, seed=22)
     f_ref, fl1 = oracle.fp8_linear(x, c8, s8)
-    check(f8_run(sk, x, c8, s8), f_ref, fl1, False, "fp8 long K")
+    with variant(sk, var):
+        check(nv_run(sk, x, codes, scales, g), y_ref, l1, False, "nvfp4 long K")
+        check(f8_run(sk, x, c8, s8), f_ref, fl1, False, "fp8 long K")
 
 
 # ------------------------------------------------- exact / bitwise cases ---
 
-@pytest.mark.parametrize("M", [1, 8])
-def test_identity_is_bitwise(sk, M):
+@pytest.mark.parametrize("M,var", ONE_AND_EIGHT)
+def test_identity_is_bitwise(sk, M, var):
+    with variant(sk, var):
+        _identity_case(sk, M)
+
+
+def _identity_case(sk, M):
     K = N = 512
     x = synth.x_f16(M, K, seed=31)
     nib = np.zeros((N, K), np.uint8)
@@ -106,8 +137,8 @@ def test_identity_is_bitwise(sk, M):
     assert np.array_equal(f8_run(sk, x, c8, s8), x.astype(np.float64))
 
 
-@pytest.mark.parametrize("M", [1, 4, 8])
-def test_every_code_byte_decodes_exactly(sk, M):
+@pytest.mark.parametrize("M,var", ONE_AND_EIGHT + [(4, "auto")])
+def test_every_code_byte_decodes_exactly(sk, M, var):
     """Row n holds code byte n at k = (0, 1) and scale code 0x38: y[m][n] =
     x[m][0]*E2M1(n & 15) + x[m][1]*E2M1(n >> 4), a sum of two exact products with
     x[1] = 1024*x[0] (powers of two), so the result is exact."""
@@ -119,11 +150,12 @@ def test_every_code_byte_decodes_exactly(sk, M):
     codes[:, 0] = np.arange(256)
     scales = np.full((N, K // 16), 0x38, np.uint8)
     y_ref, _ = oracle.nvfp4_linear(x, codes, scales, 1.0)
-    assert np.array_equal(nv_run(sk, x, codes, scales, 1.0), y_ref)
+    with variant(sk, var):
+        assert np.array_equal(nv_run(sk, x, codes, scales, 1.0), y_ref)
 
 
-@pytest.mark.parametrize("M", [1, 8])
-def test_every_scale_code_decodes_exactly(sk, M):
+@pytest.mark.parametrize("M,var", ONE_AND_EIGHT)
+def test_every_scale_code_decodes_exactly(sk, M, var):
     """Row n: code 1.0 at k = 0 and block scale code n (NaN codes give NaN)."""
     K, N = 256, 256
     x = np.zeros((M, K), np.float16)
@@ -133,14 +165,15 @@ def test_every_scale_code_decodes_exactly(sk, M):
     scales = np.zeros((N, K // 16), np.uint8)
     scales[:, 0] = np.arange(256)
     y_ref, _ = oracle.nvfp4_linear(x, codes, scales, 1.0)
-    y = nv_run(sk, x, codes, scales, 1.0)
+    with variant(sk, var):
+        y = nv_run(sk, x, codes, scales, 1.0)
     nan = np.isnan(y_ref)
     assert np.array_equal(np.isnan(y), nan)
     assert np.array_equal(y[~nan], y_ref[~nan])
 
 
-@pytest.mark.parametrize("M", [1, 8])
-def test_every_fp8_code_decodes_exactly(sk, M):
+@pytest.mark.parametrize("M,var", ONE_AND_EIGHT)
+def test_every_fp8_code_decodes_exactly(sk, M, var):
     K, N = 128, 256
     x = np.zeros((M, K), np.float16)
     x[:, 5] = np.float16(1.0)
@@ -148,7 +181,8 @@ def test_every_fp8_code_decodes_exactly(sk, M):
     codes[:, 5] = np.arange(256)
     s8 = np.array([[2.0], [0.5]], np.float32)
     y_ref, _ = oracle.fp8_linear(x, codes, s8)
-    y = f8_run(sk, x, codes, s8)
+    with variant(sk, var):
+        y = f8_run(sk, x, codes, s8)
     nan = np.isnan(y_ref)
     assert np.array_equal(np.isnan(y), nan)
     assert np.array_equal(y[~nan], y_ref[~nan])
@@ -167,6 +201,9 @@ def test_one_hot_positions_bitwise(sk, k0):
         for mm in (1, 2, 4, 8):
             y = nv_run(sk, x[:mm], codes, scales, np.float32(0.25))
             assert np.array_equal(y, y_ref[:mm]), (k0, n0, mm)
+        with variant(sk, "simt"):
+            y = nv_run(sk, x[:1], codes, scales, np.float32(0.25))
+        assert np.array_equal(y, y_ref[:1]), (k0, n0, "simt")
 
 
 # --------------------------------------------------------- invariants -----
@@ -205,18 +242,19 @@ def test_rows_independent_within_a_variant(sk):
     c8, s8 = synth.fp8_weights(N, K, seed=61)
     y8 = nv_run(sk, x, codes, scales, g)
     f8 = f8_run(sk, x, c8, s8)
-    os.environ["SK_FORCE_VARIANT"] = "mma"
+    prev = sk.set_variant(sk.VARIANT_TENSOR)
     try:
         for m in range(M):
             assert np.array_equal(nv_run(sk, x[m:m + 1], codes, scales, g)[0], y8[m])
             assert np.array_equal(f8_run(sk, x[m:m + 1], c8, s8)[0], f8[m])
+        # across variants (SIMT for one row vs MMA for eight) within twice the bound
+        sk.set_variant(sk.VARIANT_SIMT)
+        y_ref, l1 = oracle.nvfp4_linear(x, codes, scales, g)
+        for m in range(M):
+            y1 = nv_run(sk, x[m:m + 1], codes, scales, g)[0]
+            assert np.all(np.abs(y1 - y8[m]) <= 2 * oracle.tolerance(l1[m]))
     finally:
-        del os.environ["SK_FORCE_VARIANT"]
-    # across variants (SIMT for one row vs MMA for eight) within twice the bound
-    y_ref, l1 = oracle.nvfp4_linear(x, codes, scales, g)
-    for m in range(M):
-        y1 = nv_run(sk, x[m:m + 1], codes, scales, g)[0]
-        assert np.all(np.abs(y1 - y8[m]) <= 2 * oracle.tolerance(l1[m]))
+        sk.set_variant(prev)
 
 
 # ------------------------------------------------------ degenerate cases ---
