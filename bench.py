@@ -261,12 +261,18 @@ def size_oracle_sample(M, budget_s):
 
 
 def cpu_oracle_sample(M, budget_s=10.0):
-    """The CPU oracle on a bounded sample of the step (see size_oracle_sample).
-    Returns (GB/s, cols, seconds, threads)."""
+    """The CPU oracle on a bounded sample of the step (see size_oracle_sample),
+    passed over again until budget_s of CPU work is timed (the column cap keeps
+    the host-side weights of the sample near 1 GB).
+    Returns (GB/s, cols, passes, seconds, threads)."""
     import oracle
 
     sample, cols, nbytes, dt = size_oracle_sample(M, budget_s)
-    return nbytes / dt / 1e9, cols, dt, oracle.threads()
+    passes = 1
+    while dt < budget_s:
+        b, t = oracle_pass(sample)
+        nbytes, dt, passes = nbytes + b, dt + t, passes + 1
+    return nbytes / dt / 1e9, cols, passes, dt, oracle.threads()
 
 
 def run_reference(args):
@@ -454,11 +460,11 @@ def run_ours(args):
             "layers": layers,
         }
         if not args.no_cpu and world == 1:
-            gbs, cols, dt, cores = cpu_oracle_sample(M)
+            gbs, cols, passes, dt, cores = cpu_oracle_sample(M)
             line["cpu_baseline"] = {
                 "value": round(gbs, 6), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                "sample": f"{cols} output columns of each of qkv, o_proj, gate_up, down, lm_head at "
-                          f"full K, M={M}, synthetic weights; {dt:.1f} s"}
+                "sample": f"{passes} pass(es) over {cols} output columns of each of qkv, o_proj, gate_up, "
+                          f"down, lm_head at full K, M={M}, synthetic weights; {dt:.1f} s"}
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
