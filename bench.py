@@ -5,7 +5,8 @@ tokens (default 8, the k=7 speculative verify round; --m 1 for plain decode):
 
     64 x { qkv (FP8, K=5120 N=7168), o_proj (FP8, K=6144 N=5120),
            gate_up (NVFP4, K=5120 N=34816), down (NVFP4, K=17408 N=5120) }
-    + lm_head (NVFP4, K=5120 N=151936) with the fused greedy argmax
+    + lm_head (NVFP4, K=5120 N=151936) with the fused greedy argmax and, at
+      M > 1, the greedy verification of the M - 1 drafted tokens
 
 i.e. 257 calls of the C ABI, captured once into a CUDA graph and replayed.
 Weights (14.43 GB per step) are synthetic, generated on the device with the
@@ -16,8 +17,8 @@ per second.
 Also measured: the dominant kernel alone (the NVFP4 gate_up launch, rotating
 over 8 weight copies = 802 MB so L2 is cold) for the roofline, a per-layer
 table with cold L2 at M = 1 and 8, and the end-to-end rate through the C ABI
-with the activations copied from pinned host memory and the argmax read back
-every step.  --impl reference times the CPU oracle on a bounded sample.
+with the activations (and drafted tokens) copied from pinned host memory and
+the picks (and the round's verdict) read back every step.  --impl reference times the CPU oracle on a bounded sample.
 """
 from __future__ import annotations
 
@@ -157,15 +158,25 @@ class Linear:
 
 
 class LMHead(Linear):
+    """The vocabulary projection with its fused greedy pick; at M > 1 (the
+    speculative verify round) it also verifies M - 1 drafted tokens."""
+
     def __init__(self, M, gen, dev):
         import torch
 
         super().__init__(*LM_HEAD, M, gen, dev, out_f16=False)
         self.am = torch.empty((M,), dtype=torch.int32, device=dev)
+        self.draft = torch.randint(0, LM_HEAD[3], (max(M - 1, 1),), generator=gen, device=dev,
+                                   dtype=torch.int32)
+        self.accept = torch.empty((2,), dtype=torch.int32, device=dev)
 
     def call(self, sk, x=None):
-        sk.lm_head_argmax(self.x if x is None else x, self.codes, self.scales, self.g,
-                          logits=self.y, argmax=self.am)
+        x = self.x if x is None else x
+        if self.M > 1:
+            sk.lm_head_verify(x, self.codes, self.scales, self.g, self.draft, logits=self.y, argmax=self.am,
+                              accept=self.accept)
+        else:
+            sk.lm_head_argmax(x, self.codes, self.scales, self.g, logits=self.y, argmax=self.am)
 
 
 def time_graph(graph, stream, reps, warmup, barrier=None):
@@ -328,7 +339,7 @@ def aggregate(ms_local, bytes_per_rank, dist=None):
 def config(M):
     return {"workload": f"decode round: {N_LAYERS} x (qkv FP8 5120x7168, o_proj FP8 6144x5120, "
                         f"gate_up NVFP4 5120x34816, down NVFP4 17408x5120) + NVFP4 lm_head 5120x151936 "
-                        f"with fused argmax, M={M}",
+                        f"with fused argmax{' and greedy verify of the M-1 drafts' if M > 1 else ''}, M={M}",
             "M": M, "layers": N_LAYERS, "weight_bytes_per_step": STEP_BYTES,
             "l2": "inputs larger than L2 (14.4 GB of weights streamed per step), no flush needed",
             "parallelism": "replicas"}
@@ -398,8 +409,9 @@ def run_ours(args):
     if st != 0:
         raise RuntimeError(f"device error {st}")
 
-    # ---- end to end through the C ABI: activations from pinned host memory,
-    # argmax back to the host, every step
+    # ---- end to end through the C ABI: activations (and the drafted tokens of
+    # the verify round) from pinned host memory, the picks (and the round's
+    # verdict) back to the host, every step
     x_dev = torch.empty(sum(c.x.numel() for c in calls), dtype=torch.float16, device=dev)
     views, off = [], 0
     for c in calls:
@@ -407,12 +419,20 @@ def run_ours(args):
         off += c.x.numel()
     x_host = torch.randn(x_dev.numel(), generator=torch.Generator().manual_seed(7)).to(torch.float16).pin_memory()
     am_host = torch.empty((M,), dtype=torch.int32).pin_memory()
+    draft_host = head.draft.cpu().pin_memory()
+    accept_host = torch.empty((2,), dtype=torch.int32).pin_memory()
+    h2d_bytes = x_dev.numel() * 2 + (draft_host.numel() * 4 if M > 1 else 0)
+    d2h_bytes = M * 4 + (8 if M > 1 else 0)
 
     def e2e_step():
         x_dev.copy_(x_host, non_blocking=True)
+        if M > 1:
+            head.draft.copy_(draft_host, non_blocking=True)
         for c, v in zip(calls, views):
             c.call(sk, v)
         am_host.copy_(head.am, non_blocking=True)
+        if M > 1:
+            accept_host.copy_(head.accept, non_blocking=True)
 
     g2 = capture(e2e_step, stream)
     e2e_value, e2e_ms = aggregate(time_graph(g2, stream, reps=args.steps, warmup=3, barrier=barrier),
@@ -452,7 +472,7 @@ def run_ours(args):
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs)" if peak_kind == "measured"
                          else "fallback 6.8 TB/s"},
             "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
-                    "h2d_bytes_per_step": int(x_dev.numel() * 2), "d2h_bytes_per_step": int(M * 4),
+                    "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(d2h_bytes),
                     "ms_per_step": round(e2e_ms, 4)},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),

@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     last_device_error,
     lib,
     lm_head_argmax,
+    lm_head_verify,
     nvfp4_gemm,
     set_pdl,
     set_variant,

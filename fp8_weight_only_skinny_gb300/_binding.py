@@ -45,6 +45,7 @@ def _load() -> ctypes.CDLL:
         "fp8_gemm": ([p, p, p, p, i, i, i, p], i),
         "fp8_gemm_f16out": ([p, p, p, p, i, i, i, p], i),
         "lm_head_argmax": ([p, p, p, f, p, p, i, i, i, p], i),
+        "lm_head_verify": ([p, p, p, f, p, p, p, p, i, i, i, p], i),
         "sk_status_string": ([i], ctypes.c_char_p),
         "sk_last_device_error": ([p], i),
         "sk_set_pdl": ([i], i),
@@ -64,7 +65,7 @@ lib = _load()
 
 # Names declared in include/skinny.h (the tests check that each is exported).
 EXPORTS = ("sk_init", "sk_shutdown", "nvfp4_gemm", "nvfp4_gemm_f16out", "fp8_gemm",
-           "fp8_gemm_f16out", "lm_head_argmax", "sk_status_string", "sk_last_device_error",
+           "fp8_gemm_f16out", "lm_head_argmax", "lm_head_verify", "sk_status_string", "sk_last_device_error",
            "sk_set_pdl", "sk_set_variant", "sk_inject_wait_timeout", "nvfp4_gemm_noalloc", "sk_version")
 
 
@@ -180,3 +181,30 @@ def lm_head_argmax(x, W_codes, W_scales, W_gscale: float, logits=None, argmax=No
                               logits.data_ptr() if logits is not None else None, argmax.data_ptr(),
                               M, N, K, _stream_ptr(stream)), "lm_head_argmax")
     return logits, argmax
+
+
+def lm_head_verify(x, W_codes, W_scales, W_gscale: float, draft, logits=None, argmax=None, accept=None,
+                   want_logits: bool = True, stream=None):
+    """lm_head_argmax plus the greedy verification of a speculative round:
+    draft is int32 [M - 1] on the device (ignored when M == 1).
+
+    Returns (logits or None, argmax int32 [M], accept int32 [2] = (accepted drafts, bonus token))."""
+    import torch
+
+    M, N, K = _dims(x, W_codes, True)
+    if W_scales.dtype != torch.uint8 or tuple(W_scales.shape) != (N, K // 16) or not W_scales.is_contiguous():
+        raise ValueError("W_scales must be a contiguous uint8 tensor [N][K/16]")
+    if M > 1 and (draft is None or draft.dtype != torch.int32 or not draft.is_cuda or draft.numel() < M - 1
+                  or not draft.is_contiguous()):
+        raise ValueError("draft must be a contiguous CUDA int32 tensor of at least M - 1 tokens")
+    if logits is None and want_logits:
+        logits = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    if argmax is None:
+        argmax = torch.empty((M,), dtype=torch.int32, device=x.device)
+    if accept is None:
+        accept = torch.empty((2,), dtype=torch.int32, device=x.device)
+    _check(lib.lm_head_verify(x.data_ptr(), W_codes.data_ptr(), W_scales.data_ptr(), float(W_gscale),
+                              logits.data_ptr() if logits is not None else None, argmax.data_ptr(),
+                              draft.data_ptr() if (draft is not None and M > 1) else None, accept.data_ptr(),
+                              M, N, K, _stream_ptr(stream)), "lm_head_verify")
+    return logits, argmax, accept

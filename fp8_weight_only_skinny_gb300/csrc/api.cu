@@ -95,7 +95,8 @@ sk_status zero_outputs(void *y, size_t y_bytes, int32_t *argmax, int M, cudaStre
 }
 
 sk_status run(Kind kind, const void *x, const uint8_t *codes, const void *scales, float gscale, void *y,
-              int32_t *argmax, int M, int N, int K, void *stream) {
+              int32_t *argmax, int M, int N, int K, void *stream, const int32_t *draft = nullptr,
+              int32_t *accept = nullptr) {
     const bool nv = (kind == Kind::NVFP4 || kind == Kind::NVFP4_F16 || kind == Kind::LMHEAD);
     const bool f16 = (kind == Kind::NVFP4_F16 || kind == Kind::FP8_F16);
     const bool am = (kind == Kind::LMHEAD);
@@ -110,6 +111,11 @@ sk_status run(Kind kind, const void *x, const uint8_t *codes, const void *scales
     if (nv ? !aligned(scales, 16) : !aligned(scales, 4)) return SK_ERR_MISALIGNED;
     if (y && !aligned(y, f16 ? 2 : 4)) return SK_ERR_MISALIGNED;
     if (argmax && !aligned(argmax, 4)) return SK_ERR_MISALIGNED;
+    if (accept) {
+        if (M > 1 && !draft) return SK_ERR_INVALID_ARG;
+        if (K == 0) return SK_ERR_UNSUPPORTED_SHAPE;   // no logits to verify against
+        if (!aligned(accept, 4) || (draft && !aligned(draft, 4))) return SK_ERR_MISALIGNED;
+    }
     DeviceState *d = current(nullptr);
     if (!d) return SK_ERR_NOT_INITIALIZED;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -122,6 +128,8 @@ sk_status run(Kind kind, const void *x, const uint8_t *codes, const void *scales
     p.gscale = nv ? gscale : 1.0f;
     p.y = y;
     p.argmax = argmax;
+    p.draft = draft;
+    p.accept = accept;
     p.ws = d->ws;
     p.M = M;
     p.N = N;
@@ -240,6 +248,13 @@ sk_status fp8_gemm_f16out(const void *x, const uint8_t *W_codes, const float *W_
 sk_status lm_head_argmax(const void *x, const uint8_t *W_codes, const uint8_t *W_scales, float W_gscale,
                          float *logits, int32_t *argmax, int M, int N, int K, void *stream) {
     return run(Kind::LMHEAD, x, W_codes, W_scales, W_gscale, logits, argmax, M, N, K, stream);
+}
+
+sk_status lm_head_verify(const void *x, const uint8_t *W_codes, const uint8_t *W_scales, float W_gscale,
+                         float *logits, int32_t *argmax, const int32_t *draft, int32_t *accept, int M, int N,
+                         int K, void *stream) {
+    if (!accept) return SK_ERR_INVALID_ARG;
+    return run(Kind::LMHEAD, x, W_codes, W_scales, W_gscale, logits, argmax, M, N, K, stream, draft, accept);
 }
 
 const char *sk_status_string(sk_status status) {

@@ -103,6 +103,8 @@ struct Params {
     float gscale;               // NVFP4 tensor scale (1 for FP8)
     void *y;                    // [M][N] f32 or f16; may be null with ARGMAX
     int32_t *argmax;            // [M] (ARGMAX only)
+    const int32_t *draft;       // [M - 1] drafted tokens, or null (ARGMAX only)
+    int32_t *accept;            // [2] accepted drafts, bonus token; with draft (ARGMAX only)
     unsigned char *ws;          // workspace base
     int M, N, K;
     int G, C, KB;               // row groups, k-chunks, FP8 scale row stride
@@ -704,10 +706,21 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
             const unsigned int old = atomicAdd(&ctrl->done, 1u);
             if (old == gridDim.x - 1) {
                 __threadfence();
+                int pick[8];
                 for (int m = 0; m < p.M; ++m) {
                     const unsigned long long k = ld_cg_u64(&ctrl->argmax_key[m]);
-                    p.argmax[m] = static_cast<int32_t>(~static_cast<unsigned int>(k & 0xffffffffull));
+                    pick[m] = static_cast<int32_t>(~static_cast<unsigned int>(k & 0xffffffffull));
+                    p.argmax[m] = pick[m];
                     ctrl->argmax_key[m] = 0ull;
+                }
+                if (p.accept) {
+                    // Greedy verification of the speculative round: draft j is
+                    // accepted while all earlier ones were and it equals row j's
+                    // pick; the target then commits its own pick after them.
+                    int a = 0;
+                    while (a < p.M - 1 && p.draft[a] == pick[a]) ++a;
+                    p.accept[0] = a;
+                    p.accept[1] = pick[a];
                 }
                 ctrl->done = 0u;
             }

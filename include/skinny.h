@@ -143,6 +143,26 @@ SK_API sk_status lm_head_argmax(const void *x, const uint8_t *W_codes, const uin
                          float W_gscale, float *logits, int32_t *argmax,
                          int M, int N, int K, void *stream);
 
+/*
+ * lm_head_argmax plus the greedy verification of one speculative round, in the
+ * same kernel's final step (page "NVFP4 在 Volta 上！": the k = 7 MTP round is
+ * verified on eight rows, and each round commits a prefix of the drafts plus
+ * one token of the target's own).  Row m of x is the target's state after the
+ * prefix and the first m drafted tokens, so argmax[m] is the target's pick for
+ * the position that draft[m] proposes.
+ *   draft   const i32 [M - 1]: the drafted tokens (may be NULL when M == 1),
+ *           4-byte aligned, device memory
+ *   accept  i32 [2], 4-byte aligned: accept[0] = a, the number of leading
+ *           drafts with draft[j] == argmax[j] for every j < a; accept[1] =
+ *           argmax[a], the token the target commits after them (a + 1 tokens
+ *           are committed in all)
+ *   Other arguments as lm_head_argmax.  K = 0 is rejected with
+ *   SK_ERR_UNSUPPORTED_SHAPE (no logits to verify against).
+ */
+SK_API sk_status lm_head_verify(const void *x, const uint8_t *W_codes, const uint8_t *W_scales,
+                                float W_gscale, float *logits, int32_t *argmax, const int32_t *draft,
+                                int32_t *accept, int M, int N, int K, void *stream);
+
 /* Static, human-readable name of a status code. */
 SK_API const char *sk_status_string(sk_status status);
 

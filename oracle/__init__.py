@@ -14,6 +14,7 @@ from .oracle import (  # noqa: F401
     nvfp4_linear,
     fp8_linear,
     argmax_rows,
+    verify,
     tolerance,
     threads,
 )

@@ -192,6 +192,28 @@ void oracle_argmax_rows(int64_t M, int64_t N, const double *y, int64_t *idx)
     }
 }
 
+/*
+ * Greedy verification of one speculative round (page "NVFP4 在 Volta 上！":
+ * the k = 7 MTP round is verified by the target on eight rows, and a round
+ * commits a prefix of the drafts plus one token of the target's own).  Row m
+ * of the target holds its greedy pick target[m] for the position after the
+ * prefix and the first m drafts; draft[j] (j < M - 1) is the j-th drafted
+ * token.  Draft j is accepted while every draft before it was, and it equals
+ * target[j].  accept[0] = the number of accepted drafts a; accept[1] =
+ * target[a], the token the target itself commits after them.
+ */
+void oracle_verify(int64_t M, const int64_t *target, const int32_t *draft, int64_t *accept)
+{
+    int64_t a = 0;
+    for (int64_t j = 0; j < M - 1; j++) {
+        if ((int64_t)draft[j] != target[j])
+            break;
+        a = j + 1;
+    }
+    accept[0] = a;
+    accept[1] = target[a];
+}
+
 int oracle_threads(void)
 {
 #ifdef _OPENMP

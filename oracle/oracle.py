@@ -55,6 +55,8 @@ def _load():
         lib.oracle_fp8_linear.argtypes = [i64, i64, i64, p, p, p, p, i64, p, p]
         lib.oracle_argmax_rows.restype = None
         lib.oracle_argmax_rows.argtypes = [i64, i64, p, p]
+        lib.oracle_verify.restype = None
+        lib.oracle_verify.argtypes = [i64, p, p, p]
         lib.oracle_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -155,6 +157,19 @@ def argmax_rows(y) -> np.ndarray:
     idx = np.zeros(M, np.int64)
     _load().oracle_argmax_rows(M, N, _ptr(y), _ptr(idx))
     return idx
+
+
+def verify(target, draft) -> tuple:
+    """Greedy verification of a speculative round (oracle.c oracle_verify):
+    (accepted drafts a, bonus token target[a])."""
+    target = np.ascontiguousarray(target, dtype=np.int64)
+    M = target.shape[0]
+    draft = np.ascontiguousarray(np.asarray(draft, dtype=np.int32).reshape(-1)[:max(M - 1, 0)])
+    if draft.shape[0] < M - 1:
+        raise ValueError("need M - 1 draft tokens")
+    out = np.zeros(2, np.int64)
+    _load().oracle_verify(M, _ptr(target), _ptr(draft) if draft.size else None, _ptr(out))
+    return int(out[0]), int(out[1])
 
 
 def tolerance(l1, f16_out: bool = False, y_ref=None):

@@ -111,3 +111,16 @@ def test_variant_setting_round_trips_and_rejects_unknown_values():
         assert sk.set_variant(sk.VARIANT_AUTO) == sk.VARIANT_SIMT
     finally:
         sk.set_variant(prev)
+
+
+def _vf(x=A, c=A, s=A, lg=A, am=A, dr=A, ac=A, M=2, N=16, K=256):
+    return sk.lib.lm_head_verify(x, c, s, 1.0, lg, am, dr, ac, M, N, K, None)
+
+
+def test_lm_head_verify_argument_checks():
+    assert _vf(ac=None) == INVALID                 # accept is required
+    assert _vf(dr=None) == INVALID                 # drafts are required when M > 1
+    assert _vf(ac=A + 2) == MISALIGNED
+    assert _vf(dr=A + 2) == MISALIGNED
+    assert _vf(K=0) == UNSUPPORTED                 # nothing to verify against
+    assert _vf(M=9) == INVALID

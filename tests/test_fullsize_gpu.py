@@ -199,3 +199,21 @@ def test_back_to_back_bitwise(sk, fmt, M):
     else:
         y_ref, l1 = oracle.nvfp4_linear(xs[1], ws[1][0], ws[1][1], ws[1][2], cols=cols)
     check(first[:, cols], y_ref, l1, True, f"{fmt} down after gate_up M={M}")
+
+
+def test_lm_head_verify_full_size(sk):
+    """The k = 7 verify round on the full vocabulary (K=5120, N=151936, M=8):
+    every draft accepted, then the first draft rejected."""
+    import torch
+
+    K, N = synth.LM_HEAD_SHAPE
+    M = 8
+    x = synth.x_f16(M, K, seed=108)
+    codes, scales, g = _nv(N, K, 101)
+    xd, cd, sd = dev(x), dev(codes), dev(scales)
+    _, am = sk.lm_head_argmax(xd, cd, sd, float(g), want_logits=False)
+    picks = host(am).astype(np.int64)
+    for d in (picks[:7].astype(np.int32), np.concatenate([[int(picks[0] + 1) % N], picks[1:7]]).astype(np.int32)):
+        _, am2, acc = sk.lm_head_verify(xd, cd, sd, float(g), torch.from_numpy(d).to("cuda:0"), want_logits=False)
+        assert np.array_equal(host(am2), host(am))
+        assert tuple(int(v) for v in host(acc)) == oracle.verify(picks, d)

@@ -83,3 +83,36 @@ def test_repeated_argmax_is_stable(sk):
         if first is None:
             first = cur
         assert np.array_equal(cur[0], first[0]) and np.array_equal(cur[1], first[1])
+
+
+@pytest.mark.parametrize("var", ["auto", "simt"])
+@pytest.mark.parametrize("M", [1, 2, 5, 8])
+def test_verify_round(sk, M, var):
+    """lm_head_verify: the accepted count and bonus token equal the oracle's
+    greedy verification of the same call's picks, for a first rejected draft at
+    every position and for every draft accepted; the picks and logits equal
+    lm_head_argmax's bitwise and meet the oracle contract."""
+    import torch
+    from gpu_util import variant
+
+    K, N = 2048, 3001
+    x = synth.x_f16(M, K, seed=300 + M)
+    codes, scales, g = synth.nvfp4_weights(N, K, seed=301)
+    xd, cd, sd = dev(x), dev(codes), dev(scales)
+    with variant(sk, var if M == 1 else "auto"):
+        lg0, am0 = sk.lm_head_argmax(xd, cd, sd, float(g))
+        picks = host(am0).astype(np.int64)
+        y_ref, l1 = oracle.nvfp4_linear(x, codes, scales, g)
+        _argmax_ok(picks, y_ref, l1, host(lg0))
+        cases = []
+        for L in range(M):                             # drafts accepted up to L, then one rejected
+            d = picks[:M - 1].astype(np.int32).copy()
+            if L < M - 1:
+                d[L] = (d[L] + 1) % N
+            cases.append(d)
+        for d in cases:
+            dd = torch.from_numpy(np.ascontiguousarray(d) if d.size else np.zeros(1, np.int32)).to("cuda:0")
+            lg, am, acc = sk.lm_head_verify(xd, cd, sd, float(g), dd)
+            assert np.array_equal(host(am), host(am0)) and np.array_equal(host(lg), host(lg0))
+            a, bonus = oracle.verify(picks, d)
+            assert tuple(int(v) for v in host(acc)) == (a, bonus), (d, host(acc), (a, bonus))

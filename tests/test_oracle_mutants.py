@@ -41,6 +41,9 @@ MUTANTS = [
      "oracle_f16_to_f64(x[m * K + (K - 1 - k)]) *\n                           nvfp4_weight", None),
     ("l1_without_abs", "mag += fabs(p);", "mag += p;", None),
     ("argmax_ties_high", "v > y[m * N + best]", "v >= y[m * N + best]", None),
+    ("verify_count_off_by_one", "a = j + 1;", "a = j;", None),
+    ("verify_bonus_index", "accept[1] = target[a];", "accept[1] = target[a > 0 ? a - 1 : 0];", None),
+    ("verify_no_break", "            break;\n        a = j + 1;", "            continue;\n        a = j + 1;", None),
 ]
 
 

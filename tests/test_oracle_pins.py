@@ -307,3 +307,41 @@ def test_tolerance_formula():
     # one FP16 ulp at 1.0 is 2^-10, at 1000 it is 2^-1, below 2^-14 it is 2^-24
     t = oracle.tolerance(np.zeros(3), f16_out=True, y_ref=np.array([1.0, 1000.0, 1e-6]))
     assert np.allclose(t - 1e-6, [2.0 ** -10, 2.0 ** -1, 2.0 ** -24])
+
+
+# ---------------------------------------------------------- verify round ---
+
+def _committed_by_enumeration(target, draft):
+    """The committed tokens of a greedy speculative round, by direct enumeration:
+    the longest prefix of the drafts that the target would have produced itself
+    token by token, then the target's own next token."""
+    out = []
+    for j in range(len(target)):
+        out.append(int(target[j]))           # the target's pick at this position is committed
+        if j == len(target) - 1 or int(draft[j]) != int(target[j]):
+            break                            # a rejected draft ends the round after the target's pick
+    return out
+
+
+def test_verify_matches_enumeration_on_every_tiny_case():
+    """Every target and draft sequence over a two-token alphabet for M = 1..5:
+    the accepted count and bonus token reproduce the committed sequence."""
+    import itertools
+    for M in range(1, 6):
+        for target in itertools.product((0, 1), repeat=M):
+            for draft in itertools.product((0, 1), repeat=M - 1):
+                a, bonus = oracle.verify(np.array(target), np.array(draft, dtype=np.int32))
+                committed = _committed_by_enumeration(target, draft)
+                assert len(committed) == a + 1 and committed[-1] == bonus, (target, draft)
+                assert list(draft[:a]) == committed[:-1]
+
+
+def test_verify_special_cases():
+    t = np.array([7, 11, 13, 17, 19, 23, 29, 31])
+    assert oracle.verify(t, t[:7].astype(np.int32)) == (7, 31)          # every draft accepted
+    assert oracle.verify(t, np.full(7, -1, np.int32)) == (0, 7)         # first draft rejected
+    assert oracle.verify(t[:1], np.zeros(0, np.int32)) == (0, 7)       # one row: no drafts
+    for L in range(7):                                                  # first mismatch at L
+        d = t[:7].astype(np.int32).copy()
+        d[L] = 1000
+        assert oracle.verify(t, d) == (L, int(t[L]))
