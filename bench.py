@@ -39,6 +39,14 @@ LAYER = [("qkv", "fp8", 5120, 7168), ("o_proj", "fp8", 6144, 5120),
          ("gate_up", "nvfp4", 5120, 34816), ("down", "nvfp4", 17408, 5120)]
 LM_HEAD = ("lm_head", "nvfp4", 5120, 151936)
 N_LAYERS = 64
+# The pages quote their kernels at the per-rank shapes of 4-way tensor
+# parallelism: qkv, gate_up and the lm_head split over N, o_proj and down over K.
+TP_WORLD = 4
+TP_AXIS = {"qkv": "n", "o_proj": "k", "gate_up": "n", "down": "k", "lm_head": "n"}
+
+
+def tp_shape(name, K, N, world=TP_WORLD):
+    return (K, N // world) if TP_AXIS[name] == "n" else (K // world, N)
 
 
 def weight_bytes(fmt: str, K: int, N: int) -> int:
@@ -210,6 +218,22 @@ def capture(fn, stream):
     return g
 
 
+def layer_table(sk, gen, dev, stream, peak, tp=False):
+    """Per-layer cold-L2 rates at M = 1 and 8, both formats (the lm_head in
+    NVFP4), at the full shapes or at the per-rank shapes of 4-way tensor
+    parallelism."""
+    rows = []
+    for mm in (1, 8):
+        for name, f, K, N in LAYER + [LM_HEAD]:
+            Ks, Ns = tp_shape(name, K, N) if tp else (K, N)
+            for fmt in ((f,) if name == "lm_head" else ("nvfp4", "fp8")):
+                t_ms, b = cold_layer_rate(sk, fmt, Ks, Ns, mm, gen, dev, stream)
+                gbs = b / (t_ms * 1e-3) / 1e9
+                rows.append({"layer": name, "fmt": fmt, "M": mm, "K": Ks, "N": Ns, "us": round(t_ms * 1e3, 2),
+                             "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 3)})
+    return rows
+
+
 def cold_layer_rate(sk, fmt, K, N, M, gen, dev, stream, copies=None):
     """Per-launch time of one layer with a cold L2: a graph of back-to-back
     launches over enough distinct weight copies (>= 4x L2 in total)."""
@@ -368,13 +392,10 @@ def run_ours(args):
     stream = torch.cuda.Stream(device=dev)
     if args.layers_only:
         peak, _ = peaks()
-        for mm in (1, 8):
-            for name, f, K, N in LAYER + [LM_HEAD]:
-                for fmt in ((f,) if name == "lm_head" else ("nvfp4", "fp8")):
-                    t_ms, b = cold_layer_rate(sk, fmt, K, N, mm, gen, dev, stream)
-                    gbs = b / (t_ms * 1e-3) / 1e9
-                    print(f"{name:8s} {fmt:5s} M={mm}  {t_ms * 1e3:8.2f} us  {gbs:8.1f} GB/s  "
-                          f"{gbs / peak * 100:5.1f}% of peak", flush=True)
+        for tp in (False, True):
+            for r in layer_table(sk, gen, dev, stream, peak, tp=tp):
+                print(f"{'tp4 ' if tp else ''}{r['layer']:8s} {r['fmt']:5s} M={r['M']}  K={r['K']:6d} N={r['N']:6d} "
+                      f"{r['us']:8.2f} us  {r['GB/s']:8.1f} GB/s  {r['frac_of_peak'] * 100:5.1f}% of peak", flush=True)
         return
 
     # ---- the decode-round stack
@@ -445,16 +466,12 @@ def run_ours(args):
     achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
     traffic = read_traffic(M)
 
-    # ---- per-layer table, cold L2, M = 1 and 8
-    layers = []
+    # ---- per-layer tables, cold L2, M = 1 and 8: the full shapes, and the
+    # per-rank shapes of 4-way tensor parallelism (the pages' own workload)
+    layers, tp_layers = [], []
     if not args.no_layers:
-        for mm in (1, 8):
-            for name, f, K, N in LAYER + [LM_HEAD]:
-                for fmt in ((f,) if name == "lm_head" else ("nvfp4", "fp8")):
-                    t_ms, b = cold_layer_rate(sk, fmt, K, N, mm, gen, dev, stream)
-                    gbs = b / (t_ms * 1e-3) / 1e9
-                    layers.append({"layer": name, "fmt": fmt, "M": mm, "us": round(t_ms * 1e3, 2),
-                                   "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 3)})
+        layers = layer_table(sk, gen, dev, stream, peak)
+        tp_layers = layer_table(sk, gen, dev, stream, peak, tp=True)
 
     del graph, calls, lins, head
     torch.cuda.empty_cache()
@@ -478,6 +495,7 @@ def run_ours(args):
             "clocks": clk.summary(),
             "frac_of_peak": round(value / world / peak, 4),
             "layers": layers,
+            "tp4_layers": tp_layers,
         }
         if not args.no_cpu and world == 1:
             gbs, cols, passes, dt, cores = cpu_oracle_sample(M)
