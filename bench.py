@@ -234,6 +234,37 @@ def layer_table(sk, gen, dev, stream, peak, tp=False):
     return rows
 
 
+def quant_rates(sk, gen, dev, stream, peak, K=5120, N=34816, reps=10):
+    """The GPU quantizers on one FP16 weight of the gate_up shape (356 MB, far
+    above L2).  Algorithmic bytes: the FP16 weight read (twice for NVFP4, whose
+    codes need the tensor maximum first) plus the codes and scales written."""
+    import torch
+
+    w = (torch.randn((N, K), generator=gen, device=dev) * 0.02).to(torch.float16)
+    fp8_bytes = 2 * N * K + N * K + 4 * ((N + 127) // 128) * ((K + 127) // 128)
+    nv_bytes = 2 * 2 * N * K + N * K // 2 + N * K // 16 + 4
+    rows = []
+    for name, fn, b in (("fp8_quantize", lambda: sk.fp8_quantize(w), fp8_bytes),
+                        ("nvfp4_quantize", lambda: sk.nvfp4_quantize(w), nv_bytes)):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+            stream.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+            e1.synchronize()
+        us = e0.elapsed_time(e1) / reps * 1e3
+        gbs = b / (us * 1e-6) / 1e9
+        rows.append({"op": name, "K": K, "N": N, "us": round(us, 2), "bytes": b, "GB/s": round(gbs, 1),
+                     "frac_of_peak": round(gbs / peak, 3)})
+    del w
+    torch.cuda.empty_cache()
+    return rows
+
+
 def cold_layer_rate(sk, fmt, K, N, M, gen, dev, stream, copies=None):
     """Per-launch time of one layer with a cold L2: a graph of back-to-back
     launches over enough distinct weight copies (>= 4x L2 in total)."""
@@ -396,6 +427,9 @@ def run_ours(args):
             for r in layer_table(sk, gen, dev, stream, peak, tp=tp):
                 print(f"{'tp4 ' if tp else ''}{r['layer']:8s} {r['fmt']:5s} M={r['M']}  K={r['K']:6d} N={r['N']:6d} "
                       f"{r['us']:8.2f} us  {r['GB/s']:8.1f} GB/s  {r['frac_of_peak'] * 100:5.1f}% of peak", flush=True)
+        for r in quant_rates(sk, gen, dev, stream, peak):
+            print(f"{r['op']:15s} K={r['K']} N={r['N']}  {r['us']:8.2f} us  {r['GB/s']:8.1f} GB/s  "
+                  f"{r['frac_of_peak'] * 100:5.1f}% of peak", flush=True)
         return
 
     # ---- the decode-round stack
@@ -468,10 +502,11 @@ def run_ours(args):
 
     # ---- per-layer tables, cold L2, M = 1 and 8: the full shapes, and the
     # per-rank shapes of 4-way tensor parallelism (the pages' own workload)
-    layers, tp_layers = [], []
+    layers, tp_layers, quant = [], [], []
     if not args.no_layers:
         layers = layer_table(sk, gen, dev, stream, peak)
         tp_layers = layer_table(sk, gen, dev, stream, peak, tp=True)
+        quant = quant_rates(sk, gen, dev, stream, peak)
 
     del graph, calls, lins, head
     torch.cuda.empty_cache()
@@ -496,6 +531,7 @@ def run_ours(args):
             "frac_of_peak": round(value / world / peak, 4),
             "layers": layers,
             "tp4_layers": tp_layers,
+            "quantizers": quant,
         }
         if not args.no_cpu and world == 1:
             gbs, cols, passes, dt, cores = cpu_oracle_sample(M)

@@ -14,12 +14,14 @@ from ._binding import (  # noqa: F401
     VARIANT_TENSOR,
     SkinnyError,
     fp8_gemm,
+    fp8_quantize,
     init,
     last_device_error,
     lib,
     lm_head_argmax,
     lm_head_verify,
     nvfp4_gemm,
+    nvfp4_quantize,
     set_pdl,
     set_variant,
     shutdown,

@@ -46,6 +46,8 @@ def _load() -> ctypes.CDLL:
         "fp8_gemm_f16out": ([p, p, p, p, i, i, i, p], i),
         "lm_head_argmax": ([p, p, p, f, p, p, i, i, i, p], i),
         "lm_head_verify": ([p, p, p, f, p, p, p, p, i, i, i, p], i),
+        "fp8_quantize": ([p, p, p, i, i, p], i),
+        "nvfp4_quantize": ([p, p, p, p, i, i, p], i),
         "sk_status_string": ([i], ctypes.c_char_p),
         "sk_last_device_error": ([p], i),
         "sk_set_pdl": ([i], i),
@@ -65,7 +67,8 @@ lib = _load()
 
 # Names declared in include/skinny.h (the tests check that each is exported).
 EXPORTS = ("sk_init", "sk_shutdown", "nvfp4_gemm", "nvfp4_gemm_f16out", "fp8_gemm",
-           "fp8_gemm_f16out", "lm_head_argmax", "lm_head_verify", "sk_status_string", "sk_last_device_error",
+           "fp8_gemm_f16out", "lm_head_argmax", "lm_head_verify", "fp8_quantize", "nvfp4_quantize",
+           "sk_status_string", "sk_last_device_error",
            "sk_set_pdl", "sk_set_variant", "sk_inject_wait_timeout", "nvfp4_gemm_noalloc", "sk_version")
 
 
@@ -208,3 +211,36 @@ def lm_head_verify(x, W_codes, W_scales, W_gscale: float, draft, logits=None, ar
                               draft.data_ptr() if (draft is not None and M > 1) else None, accept.data_ptr(),
                               M, N, K, _stream_ptr(stream)), "lm_head_verify")
     return logits, argmax, accept
+
+
+def _weights_f16(w):
+    import torch
+
+    if w.dtype != torch.float16 or w.dim() != 2 or not w.is_cuda or not w.is_contiguous():
+        raise TypeError("w must be a contiguous 2-D CUDA float16 tensor [N][K]")
+    return int(w.shape[0]), int(w.shape[1])
+
+
+def fp8_quantize(w, stream=None):
+    """FP16 [N][K] -> (codes uint8 [N][K], scales float32 [ceil(N/128)][ceil(K/128)])."""
+    import torch
+
+    N, K = _weights_f16(w)
+    codes = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    scales = torch.empty(((N + 127) // 128, (K + 127) // 128), dtype=torch.float32, device=w.device)
+    _check(lib.fp8_quantize(w.data_ptr(), codes.data_ptr(), scales.data_ptr(), N, K, _stream_ptr(stream)),
+           "fp8_quantize")
+    return codes, scales
+
+
+def nvfp4_quantize(w, stream=None):
+    """FP16 [N][K] -> (codes uint8 [N][K/2], scales uint8 [N][K/16], tensor scale float32 [1], on the device)."""
+    import torch
+
+    N, K = _weights_f16(w)
+    codes = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
+    scales = torch.empty((N, K // 16), dtype=torch.uint8, device=w.device)
+    gscale = torch.empty((1,), dtype=torch.float32, device=w.device)
+    _check(lib.nvfp4_quantize(w.data_ptr(), codes.data_ptr(), scales.data_ptr(), gscale.data_ptr(), N, K,
+                              _stream_ptr(stream)), "nvfp4_quantize")
+    return codes, scales, gscale

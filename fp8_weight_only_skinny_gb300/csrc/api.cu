@@ -170,6 +170,11 @@ namespace sk {
 // for M = 1 the SIMT variant wins only when each CTA streams many units (FP8
 // gate_up 5120x34816 at 36 units per CTA, NVFP4 lm_head at 156), because its
 // per-unit arithmetic is lighter while its fix-up and start-up are not.
+unsigned char *current_workspace() {
+    DeviceState *d = current(nullptr);
+    return d ? d->ws : nullptr;
+}
+
 int choose_mp(int M, bool nvfp4, long long U, long long P) {
     const int v = g_variant.load(std::memory_order_relaxed);
     if (M > 1 || v == SK_VARIANT_TENSOR) return 8;

@@ -18,6 +18,9 @@ cudaError_t launch_fp8(int mp, bool f16out, const CUtensorMap &tm_codes, const P
 // Bytes of workspace-resident partial sums one unit writes (16 rows x mp tokens).
 inline size_t unit_partial_bytes(int mp) { return size_t(16) * mp * 4; }
 
+// Workspace of the current device (null before sk_init on it).
+unsigned char *current_workspace();
+
 // Token slots of the kernel variant for an M-token call of U units on a grid
 // of P CTAs: 1 (SIMT) or 8 (tensor-core), by the process-wide variant setting.
 int choose_mp(int M, bool nvfp4, long long U, long long P);

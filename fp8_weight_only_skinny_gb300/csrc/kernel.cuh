@@ -62,6 +62,7 @@ struct Ctrl {
     unsigned long long argmax_key[8];   // per token: (ordered logit << 32) | ~n
     unsigned int done;                  // CTAs finished (argmax epilogue)
     unsigned int err;                   // device error word (bit 0: a wait timed out)
+    unsigned int qamax;                 // quantizer: max |w| over the tensor (float bits)
 };
 
 enum : unsigned int { ERR_TIMEOUT = 1u };

@@ -163,6 +163,41 @@ SK_API sk_status lm_head_verify(const void *x, const uint8_t *W_codes, const uin
                                 float W_gscale, float *logits, int32_t *argmax, const int32_t *draft,
                                 int32_t *accept, int M, int N, int K, void *stream);
 
+/*
+ * Weight quantizers: FP16 -> the formats above, on the GPU (the conversion step
+ * before the linear layers; the pages convert an FP16 checkpoint to NVFP4 --
+ * v100-skinny ai-manual.ru article, section "Конвертация модели в NVFP4" -- and
+ * keep FP8 regions in FP8, page "NVFP4 在 Volta 上！", v1.1 section -- but
+ * print no rounding rules, so this library fixes them).  Every step is an IEEE
+ * binary32 operation rounded to nearest-even, in the order given; the final
+ * roundings are nearest-even, ties to the even mantissa, saturating at the
+ * format's maximum, keeping the input's sign (also for zero).  Results are
+ * therefore bit-for-bit reproducible.  w is FP16 row-major [N][K], 16-byte
+ * aligned, device memory, with finite values (infinities or NaNs give
+ * unspecified codes); outputs are device memory owned by the caller.
+ *
+ * fp8_quantize, per 128 x 128 block (the last row / column of blocks may be
+ * partial):  a = max |w| over the block;  s = a / 448 (s = 1 when a = 0);
+ * code = E4M3(w / s).
+ *   codes  u8 [N][K], 8-byte aligned;  scales f32 [ceil(N/128)][ceil(K/128)]
+ *   K % 8 == 0 (fp8_gemm itself needs K % 128 == 0).  N or K = 0: no-op.
+ */
+SK_API sk_status fp8_quantize(const void *w, uint8_t *codes, float *scales, int N, int K, void *stream);
+
+/*
+ * nvfp4_quantize, two-level scale:  A = max |w| over the tensor;
+ * G = A / 2688 (2688 = 448 * 6; G = 1 when A = 0), written to *gscale; per row
+ * and 16 consecutive k:  b = max |w| over them;  sc = E4M3((b / 6) / G);
+ * S = the value of sc;  code = E2M1(w / (S * G)) (S = 0: signed zeros).
+ *   codes  u8 [N][K/2] (low nibble = even k), 8-byte aligned
+ *   scales u8 [N][K/16];  gscale f32 [1], 4-byte aligned, device memory
+ *   K % 16 == 0 (nvfp4_gemm itself needs K % 256 == 0).  Needs sk_init() on
+ *   the current device (the tensor maximum is gathered in its workspace), and
+ *   the workspace's one-stream-at-a-time rule applies.
+ */
+SK_API sk_status nvfp4_quantize(const void *w, uint8_t *codes, uint8_t *scales, float *gscale, int N, int K,
+                                void *stream);
+
 /* Static, human-readable name of a status code. */
 SK_API const char *sk_status_string(sk_status status);
 

@@ -18,3 +18,4 @@ from .oracle import (  # noqa: F401
     tolerance,
     threads,
 )
+from .quant import e2m1_round, e4m3_round, quantize_fp8, quantize_nvfp4  # noqa: F401

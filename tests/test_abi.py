@@ -124,3 +124,15 @@ def test_lm_head_verify_argument_checks():
     assert _vf(dr=A + 2) == MISALIGNED
     assert _vf(K=0) == UNSUPPORTED                 # nothing to verify against
     assert _vf(M=9) == INVALID
+
+
+def test_quantizer_argument_checks():
+    L = sk.lib
+    assert L.fp8_quantize(A, A, A, -1, 128, None) == INVALID
+    assert L.fp8_quantize(None, A, A, 4, 128, None) == INVALID
+    assert L.fp8_quantize(A, A, A, 4, 12, None) == UNSUPPORTED        # K % 8
+    assert L.fp8_quantize(A + 8, A, A, 4, 128, None) == MISALIGNED
+    assert L.fp8_quantize(A, A, A, 0, 128, None) == OK               # empty: nothing to do
+    assert L.nvfp4_quantize(A, A, A, None, 4, 256, None) == INVALID
+    assert L.nvfp4_quantize(A, A, A, A, 4, 24, None) == UNSUPPORTED   # K % 16
+    assert L.nvfp4_quantize(A, A + 4, A, A, 4, 256, None) == MISALIGNED

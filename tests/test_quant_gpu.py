@@ -1,0 +1,108 @@
+"""GPU parity of the weight quantizers: bit-exact against the oracle
+(oracle/quant.py) on random, extreme and exactly-tied inputs, and the
+quantized weights feed the linear layers like any others."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import check, dev, host
+
+pytestmark = pytest.mark.gpu
+
+F16 = np.float16
+
+
+@pytest.fixture(scope="module")
+def sk():
+    import torch
+
+    torch.cuda.set_device(0)
+    import fp8_weight_only_skinny_gb300 as skm
+
+    skm.init()
+    yield skm
+    assert skm.last_device_error() == skm.SK_OK
+
+
+def _weights(N, K, seed, kind):
+    r = np.random.default_rng(seed)
+    if kind == "normal":
+        return (r.standard_normal((N, K)) * 0.02).astype(F16)
+    if kind == "wide":          # every FP16 magnitude class, both signs, zeros and subnormals
+        e = r.integers(-24, 15, size=(N, K)).astype(np.float64)             # finite: below 2^15
+        w = (r.uniform(1, 1.99, size=(N, K)) * np.exp2(e) * r.choice([-1, 1], size=(N, K))).astype(F16)
+        assert np.all(np.isfinite(w))
+        w.flat[r.choice(w.size, w.size // 20, replace=False)] = 0
+        w.flat[r.choice(w.size, w.size // 20, replace=False)] = -0.0
+        w.flat[:4] = [65504, -65504, 6e-8, -6e-8]
+        return w
+    raise ValueError(kind)
+
+
+@pytest.mark.parametrize("N,K", [(128, 128), (256, 1024), (300, 200), (77, 1032)])
+@pytest.mark.parametrize("kind", ["normal", "wide"])
+def test_fp8_quantize_bitexact(sk, N, K, kind):
+    w = _weights(N, K, N * K, kind)
+    codes, scales = sk.fp8_quantize(dev(w))
+    c_ref, s_ref = oracle.quantize_fp8(w)
+    assert np.array_equal(host(scales).astype(np.float32), s_ref)
+    got = host(codes)
+    assert np.array_equal(got, c_ref), int(np.sum(got != c_ref))
+
+
+@pytest.mark.parametrize("N,K", [(16, 256), (300, 512), (77, 1040), (1, 16)])
+@pytest.mark.parametrize("kind", ["normal", "wide"])
+def test_nvfp4_quantize_bitexact(sk, N, K, kind):
+    w = _weights(N, K, N + K, kind)
+    codes, scales, g = sk.nvfp4_quantize(dev(w))
+    c_ref, s_ref, g_ref = oracle.quantize_nvfp4(w)
+    assert np.float32(host(g)[0]) == g_ref
+    assert np.array_equal(host(scales), s_ref)
+    got = host(codes)
+    assert np.array_equal(got, c_ref), int(np.sum(got != c_ref))
+
+
+def test_exact_ties_round_to_even(sk):
+    # FP8: a block whose maximum is 448 has scale 1, so w / s is w itself; the
+    # midpoints between neighbouring E4M3 values that FP16 holds exactly are ties.
+    vals = oracle.e4m3_to_f64(np.arange(0x7F))
+    mids = (vals[:-1] + vals[1:]) / 2
+    mids = mids[mids.astype(F16).astype(np.float64) == mids]
+    w = np.zeros((128, 128), F16)
+    w[0, 0] = 448
+    w.flat[1:1 + mids.size] = mids
+    w.flat[200:200 + mids.size] = -mids
+    codes, scales = sk.fp8_quantize(dev(w))
+    assert np.array_equal(host(codes), oracle.quantize_fp8(w)[0])
+    # NVFP4: tensor maximum 2688 gives G = 1; a block with maximum 6 gets scale 1,
+    # so w / (S G) is w itself: the E2M1 midpoints 0.25 ... 5 are ties.
+    w = np.zeros((2, 32), F16)
+    w[0, 0] = 2688
+    ties = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0], F16)
+    w[1, 0:8], w[1, 8:16] = ties, -ties
+    codes, scales, g = sk.nvfp4_quantize(dev(w))
+    c_ref, s_ref, g_ref = oracle.quantize_nvfp4(w)
+    assert g_ref == 1.0 and s_ref[1, 0] == 0x38
+    assert np.array_equal(host(codes), c_ref) and np.array_equal(host(scales), s_ref)
+
+
+@pytest.mark.parametrize("M", [1, 8])
+def test_quantized_weights_feed_the_linears(sk, M):
+    """GPU-quantized weights through nvfp4_gemm / fp8_gemm meet the oracle
+    contract on those codes, and the product stays near the FP16 one."""
+    K, N = 2048, 384
+    w = _weights(N, K, 9, "normal")
+    x = synth.x_f16(M, K, seed=9)
+    codes, scales, g = sk.nvfp4_quantize(dev(w))
+    y = host(sk.nvfp4_gemm(dev(x), codes, scales, float(host(g)[0])))
+    y_ref, l1 = oracle.nvfp4_linear(x, host(codes), host(scales), np.float32(host(g)[0]))
+    check(y, y_ref, l1, False, "nvfp4 from the GPU quantizer")
+    c8, s8 = sk.fp8_quantize(dev(w))
+    y8 = host(sk.fp8_gemm(dev(x), c8, s8))
+    y8_ref, l18 = oracle.fp8_linear(x, host(c8), host(s8))
+    check(y8, y8_ref, l18, False, "fp8 from the GPU quantizer")
+    exact = x.astype(np.float64) @ w.astype(np.float64).T
+    scale = np.abs(x.astype(np.float64)) @ np.abs(w.astype(np.float64)).T
+    assert np.all(np.abs(y - exact) <= 0.2 * scale)          # 4-bit weights: coarse, but close
+    assert np.all(np.abs(y8 - exact) <= 0.07 * scale)        # 8-bit weights: closer
