@@ -265,6 +265,37 @@ def quant_rates(sk, gen, dev, stream, peak, K=5120, N=34816, reps=10):
     return rows
 
 
+def sampler_cost(sk, gen, dev, stream, M=8, reps=10, T=0.6, top_k=50, top_p=0.9):
+    """The full-vocabulary lm_head with the sampled pick (temperature 0.6,
+    top-k 50, top-p 0.9) against the same projection with the greedy pick, at
+    M rows, per call (the weights are far above L2)."""
+    import torch
+
+    K, N = LM_HEAD[2], LM_HEAD[3]
+    head = LMHead(M, gen, dev)
+    u = torch.rand((M,), generator=gen, device=dev)
+    tok = torch.empty((M,), dtype=torch.int32, device=dev)
+    out = {}
+    for name, fn in (("argmax", lambda: sk.lm_head_argmax(head.x, head.codes, head.scales, head.g, logits=head.y,
+                                                          argmax=head.am)),
+                     ("sample", lambda: sk.lm_head_sample(head.x, head.codes, head.scales, head.g, u, T, top_k,
+                                                          top_p, logits=head.y, token=tok))):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+            stream.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+            e1.synchronize()
+        out[name + "_us"] = round(e0.elapsed_time(e1) / reps * 1e3, 2)
+    del head
+    torch.cuda.empty_cache()
+    return {"M": M, "K": K, "N": N, "temperature": T, "top_k": top_k, "top_p": top_p, **out}
+
+
 def cold_layer_rate(sk, fmt, K, N, M, gen, dev, stream, copies=None):
     """Per-launch time of one layer with a cold L2: a graph of back-to-back
     launches over enough distinct weight copies (>= 4x L2 in total)."""
@@ -430,6 +461,7 @@ def run_ours(args):
         for r in quant_rates(sk, gen, dev, stream, peak):
             print(f"{r['op']:15s} K={r['K']} N={r['N']}  {r['us']:8.2f} us  {r['GB/s']:8.1f} GB/s  "
                   f"{r['frac_of_peak'] * 100:5.1f}% of peak", flush=True)
+        print("lm_head greedy vs sampled:", sampler_cost(sk, gen, dev, stream), flush=True)
         return
 
     # ---- the decode-round stack
@@ -502,11 +534,12 @@ def run_ours(args):
 
     # ---- per-layer tables, cold L2, M = 1 and 8: the full shapes, and the
     # per-rank shapes of 4-way tensor parallelism (the pages' own workload)
-    layers, tp_layers, quant = [], [], []
+    layers, tp_layers, quant, sampler = [], [], [], None
     if not args.no_layers:
         layers = layer_table(sk, gen, dev, stream, peak)
         tp_layers = layer_table(sk, gen, dev, stream, peak, tp=True)
         quant = quant_rates(sk, gen, dev, stream, peak)
+        sampler = sampler_cost(sk, gen, dev, stream)
 
     del graph, calls, lins, head
     torch.cuda.empty_cache()
@@ -532,6 +565,7 @@ def run_ours(args):
             "layers": layers,
             "tp4_layers": tp_layers,
             "quantizers": quant,
+            "lm_head_sampler": sampler,
         }
         if not args.no_cpu and world == 1:
             gbs, cols, passes, dt, cores = cpu_oracle_sample(M)

@@ -19,6 +19,7 @@ from ._binding import (  # noqa: F401
     last_device_error,
     lib,
     lm_head_argmax,
+    lm_head_sample,
     lm_head_verify,
     nvfp4_gemm,
     nvfp4_quantize,

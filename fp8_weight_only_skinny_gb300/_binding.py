@@ -47,6 +47,7 @@ def _load() -> ctypes.CDLL:
         "lm_head_argmax": ([p, p, p, f, p, p, i, i, i, p], i),
         "lm_head_verify": ([p, p, p, f, p, p, p, p, i, i, i, p], i),
         "fp8_quantize": ([p, p, p, i, i, p], i),
+        "lm_head_sample": ([p, p, p, f, p, p, f, i, f, p, i, i, i, p], i),
         "nvfp4_quantize": ([p, p, p, p, i, i, p], i),
         "sk_status_string": ([i], ctypes.c_char_p),
         "sk_last_device_error": ([p], i),
@@ -67,7 +68,8 @@ lib = _load()
 
 # Names declared in include/skinny.h (the tests check that each is exported).
 EXPORTS = ("sk_init", "sk_shutdown", "nvfp4_gemm", "nvfp4_gemm_f16out", "fp8_gemm",
-           "fp8_gemm_f16out", "lm_head_argmax", "lm_head_verify", "fp8_quantize", "nvfp4_quantize",
+           "fp8_gemm_f16out", "lm_head_argmax", "lm_head_verify", "lm_head_sample", "fp8_quantize",
+           "nvfp4_quantize",
            "sk_status_string", "sk_last_device_error",
            "sk_set_pdl", "sk_set_variant", "sk_inject_wait_timeout", "nvfp4_gemm_noalloc", "sk_version")
 
@@ -244,3 +246,26 @@ def nvfp4_quantize(w, stream=None):
     _check(lib.nvfp4_quantize(w.data_ptr(), codes.data_ptr(), scales.data_ptr(), gscale.data_ptr(), N, K,
                               _stream_ptr(stream)), "nvfp4_quantize")
     return codes, scales, gscale
+
+
+def lm_head_sample(x, W_codes, W_scales, W_gscale: float, u, temperature: float, top_k: int, top_p: float,
+                   logits=None, token=None, stream=None):
+    """NVFP4 vocabulary projection with a sampled pick per row (temperature /
+    top-k / top-p; u is a float32 CUDA tensor of M uniforms in [0, 1)).
+
+    Returns (logits float32 [M][N], token int32 [M])."""
+    import torch
+
+    M, N, K = _dims(x, W_codes, True)
+    if W_scales.dtype != torch.uint8 or tuple(W_scales.shape) != (N, K // 16) or not W_scales.is_contiguous():
+        raise ValueError("W_scales must be a contiguous uint8 tensor [N][K/16]")
+    if u.dtype != torch.float32 or not u.is_cuda or u.numel() < M or not u.is_contiguous():
+        raise ValueError("u must be a contiguous CUDA float32 tensor of at least M uniforms")
+    if logits is None:
+        logits = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    if token is None:
+        token = torch.empty((M,), dtype=torch.int32, device=x.device)
+    _check(lib.lm_head_sample(x.data_ptr(), W_codes.data_ptr(), W_scales.data_ptr(), float(W_gscale),
+                              logits.data_ptr(), u.data_ptr(), float(temperature), int(top_k), float(top_p),
+                              token.data_ptr(), M, N, K, _stream_ptr(stream)), "lm_head_sample")
+    return logits, token

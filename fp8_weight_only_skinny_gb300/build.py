@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libskinny.so")
-SOURCES = ["api.cu", "k_nvfp4.cu", "k_fp8.cu", "noalloc.cu", "quant.cu"]
+SOURCES = ["api.cu", "k_nvfp4.cu", "k_fp8.cu", "noalloc.cu", "quant.cu", "sample.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]
 

@@ -198,6 +198,33 @@ SK_API sk_status fp8_quantize(const void *w, uint8_t *codes, float *scales, int 
 SK_API sk_status nvfp4_quantize(const void *w, uint8_t *codes, uint8_t *scales, float *gscale, int N, int K,
                                 void *stream);
 
+/*
+ * NVFP4 vocabulary projection with a sampled pick per row: temperature, top-k
+ * and top-p, with the random draw passed in (the pages' server samples at a
+ * temperature besides the greedy pick -- page "NVFP4 在 Volta 上！", the
+ * "温度 0.6" run -- but gives no sampler, so this library fixes the usual
+ * rule).  For row m of the FP32 logits z (those of nvfp4_gemm):
+ *   1. candidates: the top_k largest z, ordered by z descending, ties by the
+ *      lower index;
+ *   2. p_j = exp((z_j - z_0) / temperature) over them (z_0 the largest);
+ *   3. keep the shortest prefix whose running sum of p reaches top_p times
+ *      the sum over all candidates (at least one candidate);
+ *   4. token[m] = the first kept candidate whose running sum exceeds u[m]
+ *      times the sum over the kept prefix.
+ *   temperature <= 0 gives the greedy pick (the first candidate).  Sums are
+ *   FP32 in a fixed order, so a call is reproducible; where u[m] lands within
+ *   FP32 rounding of a boundary, an exact-arithmetic sampler may pick the
+ *   neighbouring candidate.
+ *   logits  f32 [M][N] (written; needed as scratch), 4-byte aligned
+ *   u       const f32 [M], uniforms in [0, 1), device memory, 4-byte aligned
+ *   token   i32 [M], 4-byte aligned
+ *   1 <= top_k <= min(N, 1024) (larger: SK_ERR_UNSUPPORTED_SHAPE);
+ *   0 < top_p <= 1; other arguments as nvfp4_gemm with N, K >= 1.
+ */
+SK_API sk_status lm_head_sample(const void *x, const uint8_t *W_codes, const uint8_t *W_scales,
+                                float W_gscale, float *logits, const float *u, float temperature, int top_k,
+                                float top_p, int32_t *token, int M, int N, int K, void *stream);
+
 /* Static, human-readable name of a status code. */
 SK_API const char *sk_status_string(sk_status status);
 

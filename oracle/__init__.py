@@ -19,3 +19,4 @@ from .oracle import (  # noqa: F401
     threads,
 )
 from .quant import e2m1_round, e4m3_round, quantize_fp8, quantize_nvfp4  # noqa: F401
+from .sample import margin as sample_margin, sample, sample_row  # noqa: F401

@@ -136,3 +136,15 @@ def test_quantizer_argument_checks():
     assert L.nvfp4_quantize(A, A, A, None, 4, 256, None) == INVALID
     assert L.nvfp4_quantize(A, A, A, A, 4, 24, None) == UNSUPPORTED   # K % 16
     assert L.nvfp4_quantize(A, A + 4, A, A, 4, 256, None) == MISALIGNED
+
+
+def _smp(lg=A, u=A, tok=A, T=0.6, k=10, p=0.9, M=2, N=4096, K=256):
+    return sk.lib.lm_head_sample(A, A, A, 1.0, lg, u, T, k, p, tok, M, N, K, None)
+
+
+def test_lm_head_sample_argument_checks():
+    assert _smp(lg=None) == INVALID and _smp(u=None) == INVALID and _smp(tok=None) == INVALID
+    assert _smp(k=0) == INVALID and _smp(k=4097) == INVALID       # 1 <= top_k <= N
+    assert _smp(k=2000) == UNSUPPORTED                             # above 1024 candidates
+    assert _smp(p=0.0) == INVALID and _smp(p=1.5) == INVALID and _smp(p=float("nan")) == INVALID
+    assert _smp(u=A + 2) == MISALIGNED and _smp(tok=A + 2) == MISALIGNED
