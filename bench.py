@@ -609,19 +609,30 @@ def run_profile_case(args):
     print(f"profile case {name}:{fmt} M={args.m} K={K} N={N} copies={args.copies}: ok")
 
 
+# The sources that decide the dominant kernel's code and launch: the linear-layer
+# kernel, its PTX helpers, its instantiation and the host code that picks its
+# grid and variant.
+KERNEL_SOURCES = ("api.cu", "internal.h", "k_nvfp4.cu", "kernel.cuh", "launch.cuh", "ptx.cuh")
+
+
+def kernel_digest():
+    """sha256[:16] over KERNEL_SOURCES, in that order."""
+    import hashlib
+
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "fp8_weight_only_skinny_gb300", "csrc")
+    for n in KERNEL_SOURCES:
+        h.update(open(os.path.join(csrc, n), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def read_traffic(M):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary, if it was taken on the current kernel source (else None)."""
-    import hashlib
-
     f = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(f):
         return None
-    h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "fp8_weight_only_skinny_gb300", "csrc")
-    for n in sorted(os.listdir(csrc)):
-        h.update(open(os.path.join(csrc, n), "rb").read())
-    digest = h.hexdigest()[:16]
+    digest = kernel_digest()
     for ln in open(f):
         p = ln.split()
         if len(p) == 3 and p[0] == f"M{M}" and p[1] == digest:
