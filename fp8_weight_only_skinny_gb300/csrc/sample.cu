@@ -3,12 +3,16 @@
 // the pages describe samples at a temperature (page "NVFP4 在 Volta 上！", the
 // "温度 0.6" run) besides the greedy pick; include/skinny.h states the rule.
 //
-// One CTA of 1024 threads per row: (1) a radix select over the row's ordered
-// FP32 keys finds the top_k-th largest; (2) an index-ordered pass gathers the
-// top_k candidates (ties at the threshold taken lowest index first); (3) a
-// bitonic sort orders them by value, then index; (4) a block scan of
-// exp((z - z_max) / T) gives the running sums that decide the top-p cut and
-// the draw.
+// One thread-block cluster of SC CTAs per row, each CTA holding a contiguous
+// slice of the row (its keys cached in shared memory): (1) a radix select, 8
+// bits at a time, finds the top_k-th largest of the row's ordered FP32 keys --
+// each CTA counts its slice into a histogram, and every CTA reads all SC
+// histograms through distributed shared memory to take the same decision;
+// (2) every CTA writes its candidates (keys above that threshold, then keys
+// equal to it, lowest index first) straight into the first CTA's shared
+// memory, at offsets from the CTAs' published counts; (3) that CTA sorts them
+// by value, then index (bitonic), and (4) a block scan of exp((z - z_max) / T)
+// gives the running sums that decide the top-p cut and the draw.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -79,76 +83,180 @@ __device__ __forceinline__ float block_scan(float v, float *warp_sum) {
     return r;
 }
 
-__global__ void __launch_bounds__(ST) sample_kernel(const float *logits, int N, const float *u, float T, int top_k,
-                                                    float top_p, int32_t *token) {
-    __shared__ unsigned int hist[256];
-    __shared__ unsigned long long cand[ST];
+constexpr int SC = 8;          // CTAs per row: one portable-size cluster
+constexpr int CACHE = 49152;   // keys of a slice kept in shared memory (192 KB); the rest re-read from L2
+
+__device__ __forceinline__ unsigned int cluster_rank() {
+    unsigned int r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA in the cluster: writes before it (shared or
+// distributed shared) are visible to reads after it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The shared::cluster address of `p` (a shared variable) in CTA `rank`.
+__device__ __forceinline__ uint32_t dsmem_addr(const void *p, unsigned int rank) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ unsigned int ld_dsmem(uint32_t a) {
+    unsigned int v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_dsmem(uint32_t a, unsigned long long v) {
+    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
+}
+
+__global__ void __cluster_dims__(SC, 1, 1) __launch_bounds__(ST)
+    sample_kernel(const float *logits, int N, const float *u, float T, int top_k, float top_p, int32_t *token) {
+    extern __shared__ unsigned int skey[];           // this slice's keys (up to CACHE)
+    __shared__ unsigned int hist[2][256];            // per pass, double-buffered across the cluster
+    __shared__ unsigned long long cand[ST];          // used in the first CTA of the cluster
     __shared__ float cum[ST];
+    __shared__ unsigned long long warp_u64[8];
     __shared__ int warp_tmp[32];
     __shared__ float warp_f[32];
+    __shared__ int s_cnt[2];                         // this CTA's keys above / equal to the threshold
     __shared__ unsigned int s_prefix, s_k;
-    __shared__ int s_total, s_gt, s_eq, s_keep, s_pick;
-    const int tid = threadIdx.x;
-    const float *z = logits + size_t(blockIdx.x) * N;
+    __shared__ int s_above, s_total, s_gt, s_eq, s_gt_off, s_eq_off, s_keep, s_pick;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const unsigned int rank = cluster_rank();
+    const int row = blockIdx.x / SC;
+    const int slice = (N + SC - 1) / SC;
+    const int start = min(N, int(rank) * slice);
+    const int len = min(N, start + slice) - start;
+    const int ncache = min(len, CACHE);
+    const float *z = logits + size_t(row) * N + start;
+    auto key_at = [&](int i) -> unsigned int { return i < ncache ? skey[i] : key_of(z[i]); };
 
-    // (1) radix select, 8 bits at a time from the top: the top_k-th largest key
+    // (1) radix select over the cluster, 8 bits at a time from the top
     unsigned int prefix = 0, mask = 0, k = unsigned(top_k);
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = tid; i < 256; i += ST) hist[i] = 0u;
+    int above = 0;                                   // this CTA's keys above the prefix found so far
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        unsigned int *h = hist[pass & 1];
+        if (tid < 256) h[tid] = 0u;
         __syncthreads();
-        for (int i = tid; i < N; i += ST) {
-            const unsigned int key = key_of(z[i]);
-            if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+        // the first pass reads the row from global memory (L2) and fills the cache
+        for (int i0 = 0; i0 < len; i0 += 4 * ST) {
+            unsigned int kk[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = i0 + j * ST + tid;
+                kk[j] = i < len ? (pass == 0 ? key_of(z[i]) : key_at(i)) : 0u;
+                if (pass == 0 && i < ncache) skey[i] = kk[j];
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const bool act = i0 + j * ST + tid < len && (kk[j] & mask) == prefix;
+                if (__any_sync(0xffffffffu, act)) {
+                    const unsigned int bin = (kk[j] >> shift) & 255u;
+                    // lanes with the same bin add once (the first pass's bins are few and crowded)
+                    const unsigned int peers = __match_any_sync(0xffffffffu, act ? bin : 0xFFFFFFFFu);
+                    if (act && __ffs(peers) - 1 == lane) atomicAdd(&h[bin], unsigned(__popc(peers)));
+                }
+            }
+        }
+        cluster_sync();
+        // Thread t < 256 takes bin 255 - t: an inclusive scan over t is the
+        // suffix sum over bins, of the cluster's total (high word) and of this
+        // CTA's own count (low word).
+        unsigned long long v = 0ull, tot = 0ull, own = 0ull;
+        if (tid < 256) {
+            const unsigned int b = 255u - unsigned(tid);
+            unsigned int t = 0;
+#pragma unroll
+            for (unsigned int r = 0; r < SC; ++r) t += ld_dsmem(dsmem_addr(h + b, r));
+            tot = t;
+            own = h[b];
+            v = (tot << 32) | own;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long y = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += y;
+            }
+            if (lane == 31) warp_u64[wid] = v;
         }
         __syncthreads();
-        if (tid == 0) {
-            unsigned int acc = 0;
-            int d = 255;
-            for (; d > 0; --d) {
-                if (acc + hist[d] >= k) break;
-                acc += hist[d];
+        if (tid < 256) {
+            for (int w = 0; w < wid; ++w) v += warp_u64[w];
+            const unsigned long long s_tot = v >> 32, s_own = v & 0xFFFFFFFFull;
+            // the digit: the cluster has >= k keys at or above it, < k above it
+            if (s_tot >= k && s_tot - tot < k) {
+                s_prefix = prefix | ((255u - unsigned(tid)) << shift);
+                s_k = k - unsigned(s_tot - tot);
+                s_above = int(s_own - own);
             }
-            s_prefix = prefix | (unsigned(d) << shift);
-            s_k = k - acc;
         }
         __syncthreads();
         prefix = s_prefix;
         k = s_k;
+        above += s_above;
         mask |= 0xFFu << shift;
-        __syncthreads();
     }
-    const unsigned int thr_key = prefix;           // top_k - k keys are above it; k more equal it
+    const unsigned int thr_key = prefix;             // top_k - k keys of the row are above it, k more equal it
     const int need_eq = int(k), n_gt = top_k - int(k);
 
-    // (2) gather: every key above the threshold, then the first need_eq equal
-    // keys in index order.  Sort key: (ordered value << 32) | ~index, so that a
-    // descending sort puts larger values first and, among equals, lower indices.
+    // (2) publish this CTA's counts; candidates go to the first CTA's array
     if (tid == 0) {
+        s_cnt[0] = above;
+        s_cnt[1] = int(hist[1][thr_key & 255u]);    // the last pass's count at the final digit
         s_gt = 0;
         s_eq = 0;
     }
-    __syncthreads();
-    for (int base = 0; base < N; base += ST) {
-        const int i = base + tid;
-        const unsigned int key = i < N ? key_of(z[i]) : 0u;
-        const bool gt = i < N && key > thr_key, eq = i < N && key == thr_key;
-        const unsigned long long ck = (static_cast<unsigned long long>(key) << 32) | static_cast<unsigned int>(~i);
-        if (gt) cand[atomicAdd(&s_gt, 1)] = ck;
-        const int r = block_rank(eq, warp_tmp, &s_total);
-        const int rank = s_eq + r;
-        if (eq && rank < need_eq) cand[n_gt + rank] = ck;
-        __syncthreads();
-        if (tid == 0) s_eq += s_total;
-        __syncthreads();
+    cluster_sync();
+    if (tid == 0) {
+        int go = 0, eo = 0;
+        for (unsigned int r = 0; r < rank; ++r) {
+            go += int(ld_dsmem(dsmem_addr(&s_cnt[0], r)));
+            eo += int(ld_dsmem(dsmem_addr(&s_cnt[1], r)));
+        }
+        s_gt_off = go;
+        s_eq_off = eo;
     }
-    if (tid >= top_k) cand[tid] = 0ull;            // padding sorts last
     __syncthreads();
+    const int gt_off = s_gt_off, eq_off = s_eq_off;
+    const uint32_t lead_cand = dsmem_addr(cand, 0);
+    const bool want_eq = eq_off < need_eq;
+    for (int i0 = 0; i0 < len; i0 += ST) {
+        const int i = i0 + tid;
+        const unsigned int key = i < len ? key_at(i) : 0u;
+        const bool gt = i < len && key > thr_key, eq = want_eq && i < len && key == thr_key;
+        // sort key: (ordered value << 32) | ~index, so that a descending sort
+        // puts larger values first and, among equals, lower indices
+        const unsigned long long ck = (static_cast<unsigned long long>(key) << 32) |
+                                      static_cast<unsigned int>(~(start + i));
+        if (gt) st_dsmem(lead_cand + 8u * unsigned(gt_off + atomicAdd(&s_gt, 1)), ck);
+        if (want_eq && __syncthreads_or(eq)) {       // rank only the chunks holding a tied key
+            const int base = eq_off + s_eq;
+            const int r = base + block_rank(eq, warp_tmp, &s_total);
+            if (eq && r < need_eq) st_dsmem(lead_cand + 8u * unsigned(n_gt + r), ck);
+            __syncthreads();
+            if (tid == 0) s_eq += s_total;
+            __syncthreads();
+        }
+    }
+    cluster_sync();                                  // all candidates are in the first CTA
+    if (rank != 0) return;
 
-    // (3) bitonic sort, descending
-    for (int size = 2; size <= ST; size <<= 1) {
+    // (3) bitonic sort of the first pow2 >= top_k slots, descending
+    int P2 = 1;
+    while (P2 < top_k) P2 <<= 1;
+    if (tid >= top_k) cand[tid] = 0ull;              // padding sorts last
+    __syncthreads();
+    for (int size = 2; size <= P2; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
             const int j = tid ^ stride;
-            if (j > tid) {
+            if (tid < P2 && j > tid) {
                 const unsigned long long a = cand[tid], b = cand[j];
                 const bool desc = (tid & size) == 0;
                 if (desc ? (a < b) : (a > b)) {
@@ -163,7 +271,7 @@ __global__ void __launch_bounds__(ST) sample_kernel(const float *logits, int N, 
     // (4) weights, running sums, the top-p cut and the draw
     const float z0 = value_of(static_cast<unsigned int>(cand[0] >> 32));
     if (!(T > 0.f)) {
-        if (tid == 0) token[blockIdx.x] = int32_t(~static_cast<unsigned int>(cand[0] & 0xFFFFFFFFull));
+        if (tid == 0) token[row] = int32_t(~static_cast<unsigned int>(cand[0] & 0xFFFFFFFFull));
         return;
     }
     const float zj = value_of(static_cast<unsigned int>(cand[tid] >> 32));
@@ -177,12 +285,12 @@ __global__ void __launch_bounds__(ST) sample_kernel(const float *logits, int N, 
     if (tid < top_k && cum[tid] >= thr && (tid == 0 || cum[tid - 1] < thr)) s_keep = tid + 1;
     __syncthreads();
     const int keep = s_keep;
-    const float target = u[blockIdx.x] * cum[keep - 1];
+    const float target = u[row] * cum[keep - 1];
     if (tid == 0) s_pick = keep - 1;
     __syncthreads();
     if (tid < keep && cum[tid] > target && (tid == 0 || cum[tid - 1] <= target)) s_pick = tid;
     __syncthreads();
-    if (tid == 0) token[blockIdx.x] = int32_t(~static_cast<unsigned int>(cand[s_pick] & 0xFFFFFFFFull));
+    if (tid == 0) token[row] = int32_t(~static_cast<unsigned int>(cand[s_pick] & 0xFFFFFFFFull));
 }
 
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -202,8 +310,12 @@ sk_status lm_head_sample(const void *x, const uint8_t *W_codes, const uint8_t *W
     if (!aligned4(u) || !aligned4(token)) return SK_ERR_MISALIGNED;
     const sk_status st = nvfp4_gemm(x, W_codes, W_scales, W_gscale, logits, M, N, K, stream);
     if (st != SK_OK) return st;
-    sample_kernel<<<M, ST, 0, reinterpret_cast<cudaStream_t>(stream)>>>(logits, N, u, temperature, top_k, top_p,
-                                                                       token);
+    const int slice = (N + SC - 1) / SC;
+    const size_t smem = size_t(slice < CACHE ? slice : CACHE) * sizeof(unsigned int);
+    if (cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+        return SK_ERR_CUDA;
+    sample_kernel<<<M * SC, ST, smem, reinterpret_cast<cudaStream_t>(stream)>>>(logits, N, u, temperature, top_k,
+                                                                              top_p, token);
     return cudaGetLastError() == cudaSuccess ? SK_OK : SK_ERR_CUDA;
 }
 

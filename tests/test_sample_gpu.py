@@ -57,13 +57,32 @@ def test_sampled_pick_matches_the_oracle(sk, M, N, T, k, p):
     _check_picks(tok, logits, u, T, k, p)
 
 
-@pytest.mark.parametrize("T,k,p", [(1.0, 40, 1.0), (0.0, 12, 1.0), (0.7, 20, 0.6)])
-def test_ties_are_broken_by_the_lower_index(sk, T, k, p):
-    """Rows n and n + 7j of the weight are equal, so the logits tie in groups
-    of many: the candidates must come in index order within a tie."""
+@pytest.mark.parametrize("M,N,K,T,k,p", [(2, 400000, 256, 0.6, 50, 0.9), (2, 400000, 256, 1.0, 1024, 1.0),
+                                          (3, 5, 256, 1.0, 5, 1.0), (3, 5, 256, 0.0, 3, 1.0),
+                                          (1, 9, 256, 0.9, 9, 0.8)])
+def test_row_lengths_at_the_slice_limits(sk, M, N, K, T, k, p):
+    """A row is split over a cluster of CTAs, each keeping up to 49152 keys in
+    shared memory: rows longer than that per CTA (the rest re-read), and rows
+    shorter than the cluster (CTAs with no keys at all)."""
     import torch
 
-    M, K, N = 8, 1024, 700
+    x = synth.x_f16(M, K, seed=N + k)
+    codes, scales, g = synth.nvfp4_weights(N, K, seed=23)
+    u = np.random.default_rng(N + k).random(M).astype(np.float32)
+    lg, tok = sk.lm_head_sample(dev(x), dev(codes), dev(scales), float(g), torch.from_numpy(u).to("cuda:0"),
+                                T, k, p)
+    _check_picks(host(tok), host(lg).astype(np.float32), u, T, k, p)
+
+
+@pytest.mark.parametrize("T,k,p", [(1.0, 40, 1.0), (0.0, 12, 1.0), (0.7, 20, 0.6)])
+@pytest.mark.parametrize("N", [700, 7000])
+def test_ties_are_broken_by_the_lower_index(sk, N, T, k, p):
+    """Rows n and n + 7j of the weight are equal, so the logits tie in groups
+    of many, spread over every CTA of a row's cluster: the candidates must
+    come in index order within a tie."""
+    import torch
+
+    M, K = 8, 1024
     x = synth.x_f16(M, K, seed=3)
     base, scales_b, g = synth.nvfp4_weights(7, K, seed=4)
     codes = np.ascontiguousarray(np.tile(base, (N // 7, 1)))
