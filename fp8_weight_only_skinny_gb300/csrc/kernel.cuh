@@ -77,6 +77,7 @@ template <> struct Traits<NVFP4> {
     static constexpr int STAGES = 8;
     static constexpr int CODE_BOX_X = ROW_BYTES / 4;   // tensor map element = u32
     static constexpr int SCALE_BOX_X = SCALE_ROW / 4;
+    static constexpr int L2_AHEAD = 0;
 };
 template <> struct Traits<FP8> {
     static constexpr int ROW_BYTES = KC;
@@ -86,6 +87,11 @@ template <> struct Traits<FP8> {
     static constexpr int STAGES = 6;
     static constexpr int CODE_BOX_X = ROW_BYTES / 4;
     static constexpr int SCALE_BOX_X = 0;
+    // Past the first ring pass the producer keeps this many units prefetched
+    // into L2 ahead of the ring: six 16 KB stages are all that fit twice per
+    // SM, and two more units in flight made every FP8 layer 2-5 % faster
+    // (NVFP4, with eight stages, measured slower with any prefetch front).
+    static constexpr int L2_AHEAD = 2;
 };
 
 // Consecutive uses of a ring stage must go to the same consumer group: stage
@@ -470,8 +476,19 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
             const uint64_t pol = l2_evict_first_policy();
             int issued = 0;
             int c = c_lo, g = g_lo;                        // unit u_lo + i, stepped without division
+            int pc = c_lo, pg = g_lo, pf = 0;              // next unit to prefetch into L2 (pf = its index)
             for (int i = 0; i < (p.stall ? 0 : n_units); ++i, step_unit(c, g, 1, p.G)) {
                 const int s = i % T::STAGES;
+                if constexpr (T::L2_AHEAD > 0) {
+                    if (i >= T::STAGES) {
+                        if (pf == 0) {
+                            pf = i;
+                            step_unit(pc, pg, i, p.G);
+                        }
+                        for (; pf < n_units && pf < i + T::L2_AHEAD; ++pf, step_unit(pc, pg, 1, p.G))
+                            tma_prefetch_l2_2d(&tm_codes, pc * T::CODE_BOX_X, pg * RG, pol);
+                    }
+                }
                 // Start-up pacing: during the first pass over the ring copy i
                 // waits until copy i - START_INFLIGHT has landed.  When every CTA
                 // asks for its whole ring at once, HBM serves the burst in no
