@@ -89,12 +89,18 @@ def quantize_fp8(w):
     return codes, scales
 
 
-def quantize_nvfp4(w):
+def quantize_nvfp4(w, amax=None):
     """FP16 [N][K] (K % 16 == 0) -> (codes u8 [N][K/2], low nibble = even k;
-    scales u8 [N][K/16]; tensor scale float32)."""
+    scales u8 [N][K/16]; tensor scale float32).
+
+    amax: max |w| over the whole tensor when w holds only some of its rows
+    (default: taken from w itself)."""
     w = np.asarray(w, dtype=np.float16).astype(_F32)
     N, K = w.shape
-    A = _F32(np.max(np.abs(w))) if w.size else _F32(0.0)
+    if amax is not None:
+        A = _F32(amax)
+    else:
+        A = _F32(np.max(np.abs(w))) if w.size else _F32(0.0)
     G = _F32(A / _F32(2688.0)) if A > 0 else _F32(1.0)
     blocks = w.reshape(N, K // 16, 16)
     b = np.max(np.abs(blocks), axis=2).astype(_F32)

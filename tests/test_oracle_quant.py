@@ -107,3 +107,19 @@ def test_nvfp4_quantizer_error_bound():
     # every element lands within one code step (2 * S * g) of its value, and within 1/3 of the block max
     assert np.all(np.abs(deq - wf) <= np.repeat(S, 16, 1) * float(g) * 1.0 + 1e-12)
     assert np.all(np.abs(deq - wf) <= b / 3 + 1e-12)
+
+
+def test_nvfp4_rows_with_the_tensor_maximum_match_the_whole_tensor():
+    """Quantizing a subset of rows, given the whole tensor's maximum, gives those
+    rows of the whole tensor's result (what the full-size GPU test relies on)."""
+    w = (np.random.default_rng(8).standard_normal((64, 256)) * 0.02).astype(np.float16)
+    w[7, 3] = -0.5
+    codes, scales, g = oracle.quantize_nvfp4(w)
+    rows = np.array([0, 7, 40, 63])
+    c2, s2, g2 = oracle.quantize_nvfp4(w[rows], amax=np.max(np.abs(w.astype(F32))))
+    assert g2 == g
+    assert np.array_equal(c2, codes[rows]) and np.array_equal(s2, scales[rows])
+    c3, s3, g3 = oracle.quantize_nvfp4(w[rows])            # without it: the subset's own maximum
+    assert g3 == g                                          # row 7 holds the maximum here
+    c4, _, g4 = oracle.quantize_nvfp4(w[[0, 40]])
+    assert g4 != g

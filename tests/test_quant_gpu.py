@@ -63,6 +63,51 @@ def test_nvfp4_quantize_bitexact(sk, N, K, kind):
     assert np.array_equal(got, c_ref), int(np.sum(got != c_ref))
 
 
+def _full_size_weight():
+    """One FP16 weight of the gate_up shape (34816 x 5120) the benchmark times,
+    N(0, 0.02) with a few extremes planted in known places."""
+    N, K = 34816, 5120
+    w = (np.random.default_rng(91).standard_normal((N, K), dtype=np.float32) * 0.02).astype(F16)
+    w[0, :4] = [0.5, -0.75, 0.0, -0.0]
+    w[N - 1, K - 16:] = 0                       # an all-zero 16-block in the last row
+    w[12345, 678] = -3.0                        # the tensor maximum
+    return w
+
+
+def test_fp8_quantize_full_size_sampled_blocks(sk):
+    """The full gate_up weight through the GPU quantizer, 48 of its 128 x 128
+    blocks (corners included) checked bitwise against the oracle."""
+    w = _full_size_weight()
+    N, K = w.shape
+    codes, scales = sk.fp8_quantize(dev(w))
+    codes, scales = host(codes), host(scales).astype(np.float32)
+    nb, kb = N // 128, K // 128
+    r = np.random.default_rng(5)
+    blocks = {(0, 0), (nb - 1, kb - 1), (0, kb - 1), (nb - 1, 0), (96, 5)}
+    while len(blocks) < 48:
+        blocks.add((int(r.integers(nb)), int(r.integers(kb))))
+    for i, j in sorted(blocks):
+        blk = w[i * 128:(i + 1) * 128, j * 128:(j + 1) * 128]
+        c_ref, s_ref = oracle.quantize_fp8(blk)
+        assert scales[i, j] == s_ref[0, 0], (i, j)
+        assert np.array_equal(codes[i * 128:(i + 1) * 128, j * 128:(j + 1) * 128], c_ref), (i, j)
+
+
+def test_nvfp4_quantize_full_size_sampled_rows(sk):
+    """The full gate_up weight through the GPU quantizer: the tensor scale, and
+    64 sampled rows (first, last, the maximum's) bitwise against the oracle
+    given the whole tensor's maximum."""
+    w = _full_size_weight()
+    N, K = w.shape
+    codes, scales, g = sk.nvfp4_quantize(dev(w))
+    amax = np.float32(np.max(np.abs(w.astype(np.float32))))
+    rows = np.unique(np.concatenate([[0, 12345, N - 1], np.random.default_rng(6).choice(N, 61, replace=False)]))
+    c_ref, s_ref, g_ref = oracle.quantize_nvfp4(w[rows], amax=amax)
+    assert np.float32(host(g)[0]) == g_ref == np.float32(np.float32(3.0) / np.float32(2688.0))
+    assert np.array_equal(host(scales)[rows], s_ref)
+    assert np.array_equal(host(codes)[rows], c_ref)
+
+
 def test_exact_ties_round_to_even(sk):
     # FP8: a block whose maximum is 448 has scale 1, so w / s is w itself; the
     # midpoints between neighbouring E4M3 values that FP16 holds exactly are ties.
