@@ -4,15 +4,18 @@
 // "温度 0.6" run) besides the greedy pick; include/skinny.h states the rule.
 //
 // One thread-block cluster of SC CTAs per row, each CTA holding a contiguous
-// slice of the row (its keys cached in shared memory): (1) a radix select, 8
-// bits at a time, finds the top_k-th largest of the row's ordered FP32 keys --
-// each CTA counts its slice into a histogram, and every CTA reads all SC
-// histograms through distributed shared memory to take the same decision;
-// (2) every CTA writes its candidates (keys above that threshold, then keys
-// equal to it, lowest index first) straight into the first CTA's shared
-// memory, at offsets from the CTAs' published counts; (3) that CTA sorts them
-// by value, then index (bitonic), and (4) a block scan of exp((z - z_max) / T)
-// gives the running sums that decide the top-p cut and the draw.
+// slice of the row (copied into shared memory with every copy in flight at
+// once): (1) a radix select, 8 bits at a time, finds the top_k-th largest of
+// the row's ordered FP32 keys -- each CTA counts its slice into a histogram,
+// and every CTA sums all SC histograms through distributed shared memory (two
+// remote reads per thread) to take the same decision; (2) every CTA writes its
+// candidates (keys above that threshold, then keys equal to it, lowest index
+// first) straight into the first CTA's shared memory, at offsets from the
+// CTAs' published counts, each thread scanning one contiguous run of keys;
+// (3) that CTA sorts them by value, then index (bitonic: stages within a warp
+// through register shuffles, the others through shared memory), and (4) a
+// block scan of exp((z - z_max) / T) gives the running sums that decide the
+// top-p cut and the draw.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -32,27 +35,31 @@ __device__ __forceinline__ float value_of(unsigned int k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// Exclusive prefix count of `flag` over the CTA, in thread order; the sum goes
-// to *total (shared memory), readable by every thread on return.
-__device__ __forceinline__ int block_rank(bool flag, int *warp_tot, int *total) {
+// Exclusive prefix sum of v over the CTA, in thread order; the sum goes to
+// *total (shared memory), readable by every thread on return.
+__device__ __forceinline__ int block_excl_scan(int v, int *warp_tot, int *total) {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const unsigned int b = __ballot_sync(0xffffffffu, flag);
-    const int in_warp = __popc(b & ((1u << lane) - 1u));
-    if (lane == 0) warp_tot[wid] = __popc(b);
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[wid] = x;
     __syncthreads();
     if (wid == 0) {
-        const int v = warp_tot[lane];
-        int x = v;
+        const int w = warp_tot[lane];
+        int t = w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
+            const int y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
         }
-        warp_tot[lane] = x - v;               // exclusive
-        if (lane == 31) *total = x;
+        warp_tot[lane] = t - w;               // exclusive over warps
+        if (lane == 31) *total = t;
     }
     __syncthreads();
-    const int r = warp_tot[wid] + in_warp;
+    const int r = warp_tot[wid] + x - v;
     __syncthreads();
     return r;
 }
@@ -116,10 +123,30 @@ __device__ __forceinline__ void st_dsmem(uint32_t a, unsigned long long v) {
     asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
 }
 
+// 4-byte asynchronous copy global -> shared; cp_async_wait_all waits for all
+// of the thread's copies.
+__device__ __forceinline__ void cp_async4(void *dst_smem, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(static_cast<uint32_t>(
+                     __cvta_generic_to_shared(dst_smem))),
+                 "l"(src)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Candidate sort key: (ordered value << 32) | ~index, so that a descending
+// sort puts larger values first and, among equals, lower indices.
+__device__ __forceinline__ unsigned long long cand_key(unsigned int key, int index) {
+    return (static_cast<unsigned long long>(key) << 32) | static_cast<unsigned int>(~index);
+}
+
+static_assert(ST == 4 * 256 && SC == 8, "the histogram merge gives each thread two of the eight ranks");
+
 __global__ void __cluster_dims__(SC, 1, 1) __launch_bounds__(ST)
     sample_kernel(const float *logits, int N, const float *u, float T, int top_k, float top_p, int32_t *token) {
-    extern __shared__ unsigned int skey[];           // this slice's keys (up to CACHE)
+    extern __shared__ unsigned int skey[];           // this slice's FP32 bits (up to CACHE)
     __shared__ unsigned int hist[2][256];            // per pass, double-buffered across the cluster
+    __shared__ unsigned int part[4][256];            // cluster totals of one pass, two ranks per row
     __shared__ unsigned long long cand[ST];          // used in the first CTA of the cluster
     __shared__ float cum[ST];
     __shared__ unsigned long long warp_u64[8];
@@ -127,7 +154,7 @@ __global__ void __cluster_dims__(SC, 1, 1) __launch_bounds__(ST)
     __shared__ float warp_f[32];
     __shared__ int s_cnt[2];                         // this CTA's keys above / equal to the threshold
     __shared__ unsigned int s_prefix, s_k;
-    __shared__ int s_above, s_total, s_gt, s_eq, s_gt_off, s_eq_off, s_keep, s_pick;
+    __shared__ int s_above, s_total, s_gt, s_gt_off, s_eq_off, s_keep, s_pick;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const unsigned int rank = cluster_rank();
     const int row = blockIdx.x / SC;
@@ -136,7 +163,10 @@ __global__ void __cluster_dims__(SC, 1, 1) __launch_bounds__(ST)
     const int len = min(N, start + slice) - start;
     const int ncache = min(len, CACHE);
     const float *z = logits + size_t(row) * N + start;
-    auto key_at = [&](int i) -> unsigned int { return i < ncache ? skey[i] : key_of(z[i]); };
+    for (int i = tid; i < ncache; i += ST) cp_async4(skey + i, z + i);
+    cp_async_wait_all();
+    __syncthreads();
+    auto key_at = [&](int i) -> unsigned int { return key_of(i < ncache ? __uint_as_float(skey[i]) : z[i]); };
 
     // (1) radix select over the cluster, 8 bits at a time from the top
     unsigned int prefix = 0, mask = 0, k = unsigned(top_k);
@@ -146,14 +176,12 @@ __global__ void __cluster_dims__(SC, 1, 1) __launch_bounds__(ST)
         unsigned int *h = hist[pass & 1];
         if (tid < 256) h[tid] = 0u;
         __syncthreads();
-        // the first pass reads the row from global memory (L2) and fills the cache
         for (int i0 = 0; i0 < len; i0 += 4 * ST) {
             unsigned int kk[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int i = i0 + j * ST + tid;
-                kk[j] = i < len ? (pass == 0 ? key_of(z[i]) : key_at(i)) : 0u;
-                if (pass == 0 && i < ncache) skey[i] = kk[j];
+                kk[j] = i < len ? key_at(i) : 0u;
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -167,16 +195,20 @@ __global__ void __cluster_dims__(SC, 1, 1) __launch_bounds__(ST)
             }
         }
         cluster_sync();
+        {
+            // every thread reads one bin of two ranks (both loads in flight together)
+            const unsigned int b = unsigned(tid) & 255u, r0 = unsigned(tid) >> 8;
+            const unsigned int v0 = ld_dsmem(dsmem_addr(h + b, r0)), v1 = ld_dsmem(dsmem_addr(h + b, r0 + 4));
+            part[r0][b] = v0 + v1;
+        }
+        __syncthreads();
         // Thread t < 256 takes bin 255 - t: an inclusive scan over t is the
         // suffix sum over bins, of the cluster's total (high word) and of this
         // CTA's own count (low word).
         unsigned long long v = 0ull, tot = 0ull, own = 0ull;
         if (tid < 256) {
             const unsigned int b = 255u - unsigned(tid);
-            unsigned int t = 0;
-#pragma unroll
-            for (unsigned int r = 0; r < SC; ++r) t += ld_dsmem(dsmem_addr(h + b, r));
-            tot = t;
+            tot = (unsigned long long)part[0][b] + part[1][b] + part[2][b] + part[3][b];
             own = h[b];
             v = (tot << 32) | own;
 #pragma unroll
@@ -211,62 +243,74 @@ __global__ void __cluster_dims__(SC, 1, 1) __launch_bounds__(ST)
         s_cnt[0] = above;
         s_cnt[1] = int(hist[1][thr_key & 255u]);    // the last pass's count at the final digit
         s_gt = 0;
-        s_eq = 0;
     }
     cluster_sync();
-    if (tid == 0) {
+    if (tid < 32) {                                  // lane r < rank reads rank r's counts
         int go = 0, eo = 0;
-        for (unsigned int r = 0; r < rank; ++r) {
-            go += int(ld_dsmem(dsmem_addr(&s_cnt[0], r)));
-            eo += int(ld_dsmem(dsmem_addr(&s_cnt[1], r)));
+        if (tid < int(rank)) {
+            go = int(ld_dsmem(dsmem_addr(&s_cnt[0], unsigned(tid))));
+            eo = int(ld_dsmem(dsmem_addr(&s_cnt[1], unsigned(tid))));
         }
-        s_gt_off = go;
-        s_eq_off = eo;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            go += __shfl_xor_sync(0xffffffffu, go, o);
+            eo += __shfl_xor_sync(0xffffffffu, eo, o);
+        }
+        if (tid == 0) {
+            s_gt_off = go;
+            s_eq_off = eo;
+        }
     }
     __syncthreads();
     const int gt_off = s_gt_off, eq_off = s_eq_off;
     const uint32_t lead_cand = dsmem_addr(cand, 0);
-    const bool want_eq = eq_off < need_eq;
-    for (int i0 = 0; i0 < len; i0 += ST) {
-        const int i = i0 + tid;
-        const unsigned int key = i < len ? key_at(i) : 0u;
-        const bool gt = i < len && key > thr_key, eq = want_eq && i < len && key == thr_key;
-        // sort key: (ordered value << 32) | ~index, so that a descending sort
-        // puts larger values first and, among equals, lower indices
-        const unsigned long long ck = (static_cast<unsigned long long>(key) << 32) |
-                                      static_cast<unsigned int>(~(start + i));
-        if (gt) st_dsmem(lead_cand + 8u * unsigned(gt_off + atomicAdd(&s_gt, 1)), ck);
-        if (want_eq && __syncthreads_or(eq)) {       // rank only the chunks holding a tied key
-            const int base = eq_off + s_eq;
-            const int r = base + block_rank(eq, warp_tmp, &s_total);
-            if (eq && r < need_eq) st_dsmem(lead_cand + 8u * unsigned(n_gt + r), ck);
-            __syncthreads();
-            if (tid == 0) s_eq += s_total;
-            __syncthreads();
+    // Each thread scans one contiguous run of the slice, so that index order
+    // within a thread and thread order agree for the tied keys.
+    const int per = (len + ST - 1) / ST;
+    const int i_lo = min(len, tid * per), i_hi = min(len, i_lo + per);
+    int n_eq = 0;
+    for (int i = i_lo; i < i_hi; ++i) {
+        const unsigned int key = key_at(i);
+        if (key > thr_key) st_dsmem(lead_cand + 8u * unsigned(gt_off + atomicAdd(&s_gt, 1)), cand_key(key, start + i));
+        n_eq += key == thr_key;
+    }
+    if (eq_off < need_eq) {                          // the same for every thread of the CTA
+        int r = eq_off + block_excl_scan(n_eq, warp_tmp, &s_total);
+        for (int i = i_lo; i < i_hi && n_eq > 0 && r < need_eq; ++i) {
+            if (key_at(i) == thr_key) {
+                st_dsmem(lead_cand + 8u * unsigned(n_gt + r), cand_key(thr_key, start + i));
+                ++r;
+            }
         }
     }
     cluster_sync();                                  // all candidates are in the first CTA
     if (rank != 0) return;
 
-    // (3) bitonic sort of the first pow2 >= top_k slots, descending
+    // (3) bitonic sort of the first pow2 >= top_k slots, descending; thread t
+    // holds slot t, exchanging with slot t ^ stride through a shuffle within a
+    // warp and through shared memory across warps
     int P2 = 1;
     while (P2 < top_k) P2 <<= 1;
-    if (tid >= top_k) cand[tid] = 0ull;              // padding sorts last
-    __syncthreads();
+    unsigned long long v = tid < top_k ? cand[tid] : 0ull;     // padding sorts last
     for (int size = 2; size <= P2; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            const int j = tid ^ stride;
-            if (tid < P2 && j > tid) {
-                const unsigned long long a = cand[tid], b = cand[j];
-                const bool desc = (tid & size) == 0;
-                if (desc ? (a < b) : (a > b)) {
-                    cand[tid] = b;
-                    cand[j] = a;
-                }
+            unsigned long long w;
+            if (stride >= 32) {
+                __syncthreads();
+                cand[tid] = v;
+                __syncthreads();
+                w = cand[tid ^ stride];
+            } else {
+                w = __shfl_xor_sync(0xffffffffu, v, stride);
             }
-            __syncthreads();
+            const bool desc = (tid & size) == 0, lower = (tid & stride) == 0;
+            const unsigned long long hi = v > w ? v : w, lo = v > w ? w : v;
+            v = desc == lower ? hi : lo;
         }
     }
+    __syncthreads();
+    cand[tid] = v;
+    __syncthreads();
 
     // (4) weights, running sums, the top-p cut and the draw
     const float z0 = value_of(static_cast<unsigned int>(cand[0] >> 32));
