@@ -79,6 +79,19 @@ def test_fp8_quantizer_error_bound_and_extremes():
     assert np.all(np.abs(deq - wf) <= bound * 1.0000001)
 
 
+def test_fp8_all_zero_block_gets_scale_one():
+    """Reading of the quantization rule: an all-zero 128 x 128 block has scale
+    1 (not 0, which would divide by zero) and zero codes, signs kept."""
+    w = (np.random.default_rng(9).standard_normal((128, 256)) * 0.02).astype(np.float16)
+    w[:, :128] = 0
+    w[5, 7] = -0.0
+    codes, scales = oracle.quantize_fp8(w)
+    assert scales[0, 0] == F32(1.0) and scales[0, 1] != F32(1.0)
+    expect = np.zeros((128, 128), np.uint8)
+    expect[5, 7] = 0x80
+    assert np.array_equal(codes[:, :128], expect)
+
+
 def test_nvfp4_quantizer_closed_forms():
     w = np.zeros((4, 64), np.float16)
     w[1, 5] = -3.0                       # the tensor maximum

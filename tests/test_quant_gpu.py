@@ -63,6 +63,18 @@ def test_nvfp4_quantize_bitexact(sk, N, K, kind):
     assert np.array_equal(got, c_ref), int(np.sum(got != c_ref))
 
 
+def test_fp8_all_zero_block(sk):
+    """An all-zero 128 x 128 block: scale 1 and zero codes (signs kept), as the oracle."""
+    w = (np.random.default_rng(9).standard_normal((256, 384)) * 0.02).astype(F16)
+    w[128:, 128:256] = 0
+    w[130, 131] = -0.0
+    codes, scales = sk.fp8_quantize(dev(w))
+    c_ref, s_ref = oracle.quantize_fp8(w)
+    assert s_ref[1, 1] == 1.0
+    assert np.array_equal(host(scales).astype(np.float32), s_ref)
+    assert np.array_equal(host(codes), c_ref)
+
+
 def _full_size_weight():
     """One FP16 weight of the gate_up shape (34816 x 5120) the benchmark times,
     N(0, 0.02) with a few extremes planted in known places."""
