@@ -677,6 +677,26 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
         // that up to 32 loads are in flight per thread.
         constexpr int CB = 8;
         const int o = ct % NOUT;
+        if (p.C > CB) {
+            // Many chunks (down: 17): one row group at a time with up to 24 of
+            // its partials in flight -- one round trip to L2 instead of three
+            // (measured: down 13.99 -> 13.38 us per launch at M = 8).
+            constexpr int CL = 24;
+            for (int e = ct / NOUT; e < n_own; e += ES) {
+                const int gq = int(blockIdx.x) + e * P;
+                float acc = 0.f;
+                for (int c0 = 0; c0 < p.C; c0 += CL) {
+                    float v[CL];
+#pragma unroll
+                    for (int k = 0; k < CL; ++k)
+                        v[k] = c0 + k < p.C ? ld_cg_f32(partials + ((size_t)gq * p.C + c0 + k) * NOUT + o) : 0.f;
+#pragma unroll
+                    for (int k = 0; k < CL; ++k)
+                        if (c0 + k < p.C) acc += v[k];
+                }
+                finalize<FMT, MP, F16OUT, ARGMAX>(p, gq, o, acc, best);
+            }
+        } else
         for (int e = ct / NOUT; e < n_own; e += 4 * ES) {
             int gg[4];
             float acc[4];
