@@ -183,6 +183,13 @@ __device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int *p) {
     return v;
 }
 
+// Release reduction at GPU scope: after a CTA barrier, it orders every store
+// the CTA made before the barrier ahead of the increment (the release is
+// cumulative over what the barrier made visible to this thread).
+__device__ __forceinline__ void red_release_add_u32(unsigned int *p, unsigned int v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // Bring the line holding `p` into L1 (no register, no wait).
 __device__ __forceinline__ void prefetch_l1(const void *p) {
     asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
