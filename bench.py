@@ -556,9 +556,10 @@ def run_ours(args):
     traffic = read_traffic(M)
 
     # ---- per-layer tables, cold L2, M = 1 and 8: the full shapes, and the
-    # per-rank shapes of 4-way tensor parallelism (the pages' own workload)
+    # per-rank shapes of 4-way tensor parallelism (the pages' own workload);
+    # single-GPU runs only (every replica would measure the same)
     layers, tp_layers, quant, sampler = [], [], [], None
-    if not args.no_layers:
+    if not args.no_layers and world == 1:
         layers = layer_table(sk, gen, dev, stream, peak)
         tp_layers = layer_table(sk, gen, dev, stream, peak, tp=True)
         quant = quant_rates(sk, gen, dev, stream, peak)
