@@ -44,7 +44,11 @@
  *       |y - y_exact| <= 1e-3 * sum_k |x[m][k] * w[n][k]| + 1e-6
  *     plus one FP16 ulp of the result for the *_f16out variants.
  *   - One stream at a time per workspace: calls whose kernels overlap in time
- *     on different streams of the same device race on the workspace.
+ *     on different streams of the same device race on the workspace.  Each
+ *     kernel also expects its whole grid (two CTAs per SM) to be resident at
+ *     once -- its split-K owners wait on the other CTAs of the grid -- so
+ *     another kernel that occupies SMs at the same time can make those waits
+ *     run out (SK_ERR_TIMEOUT) instead of finishing.
  *     Consecutive calls on one stream may overlap through programmatic
  *     dependent launch: a kernel may start streaming its own weights while the
  *     previous kernel of this library finishes, but touches x, y and the
