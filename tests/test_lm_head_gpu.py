@@ -4,7 +4,7 @@ import pytest
 
 import oracle
 import synth
-from gpu_util import check, dev, host
+from gpu_util import Guarded, argmax_ok, check, dev, host
 
 pytestmark = pytest.mark.gpu
 
@@ -24,18 +24,18 @@ def sk():
 def _argmax_ok(am, y_ref, l1, logits_gpu):
     """The fused index is the lowest-index max of the same call's FP32 logits
     (bitwise), and agrees with the oracle where its top-2 gap exceeds the bound."""
-    M = y_ref.shape[0]
-    tol = oracle.tolerance(l1)
-    for m in range(M):
-        assert am[m] == int(np.argmax(logits_gpu[m])), m
-        a = int(oracle.argmax_rows(y_ref[m:m + 1])[0])
-        order = np.argsort(-y_ref[m], kind="stable")
-        b = int(order[1]) if order[0] == a else int(order[0])
-        if y_ref[m, a] - y_ref[m, b] > tol[m, a] + tol[m, b]:
-            assert am[m] == a, (m, am[m], a)
-        else:
-            i = am[m]
-            assert y_ref[m, i] >= y_ref[m, a] - tol[m, a] - tol[m, i]
+    argmax_ok(am, y_ref, l1, logits_gpu)
+
+
+def _guarded_head(sk, x, codes, scales, g, M, N, want_logits=True):
+    """lm_head_argmax into guarded logits / argmax buffers; returns host copies."""
+    import torch
+
+    lg = Guarded((M, N), torch.float32) if want_logits else None
+    am = Guarded((M,), torch.int32, fill=-7)
+    sk.lm_head_argmax(dev(x), dev(codes), dev(scales), float(g), logits=lg.t if lg else None, argmax=am.t,
+                      want_logits=want_logits)
+    return (lg.host("logits") if lg else None), am.host("argmax")
 
 
 @pytest.mark.parametrize("M", [1, 2, 4, 8])
@@ -44,13 +44,12 @@ def test_lm_head_logits_and_argmax(sk, M, K, N):
     x = synth.x_f16(M, K, seed=M * 31 + N)
     codes, scales, g = synth.nvfp4_weights(N, K, seed=N)
     y_ref, l1 = oracle.nvfp4_linear(x, codes, scales, g)
-    logits, am = sk.lm_head_argmax(dev(x), dev(codes), dev(scales), float(g))
-    lg = host(logits)
+    lg, am = _guarded_head(sk, x, codes, scales, g, M, N)
     check(lg, y_ref, l1, False, "lm_head logits")
-    _argmax_ok(host(am), y_ref, l1, lg)
+    _argmax_ok(am, y_ref, l1, lg)
     # without logits: same indices
-    _, am2 = sk.lm_head_argmax(dev(x), dev(codes), dev(scales), float(g), want_logits=False)
-    assert np.array_equal(host(am2), host(am))
+    _, am2 = _guarded_head(sk, x, codes, scales, g, M, N, want_logits=False)
+    assert np.array_equal(am2, am)
 
 
 def test_ties_go_to_the_lowest_index(sk):
@@ -112,7 +111,11 @@ def test_verify_round(sk, M, var):
             cases.append(d)
         for d in cases:
             dd = torch.from_numpy(np.ascontiguousarray(d) if d.size else np.zeros(1, np.int32)).to("cuda:0")
-            lg, am, acc = sk.lm_head_verify(xd, cd, sd, float(g), dd)
-            assert np.array_equal(host(am), host(am0)) and np.array_equal(host(lg), host(lg0))
+            glg = Guarded((M, N), torch.float32)
+            gam = Guarded((M,), torch.int32, fill=-7)
+            gacc = Guarded((2,), torch.int32, fill=-7)
+            sk.lm_head_verify(xd, cd, sd, float(g), dd, logits=glg.t, argmax=gam.t, accept=gacc.t)
+            lg, am, acc = glg.host("logits"), gam.host("argmax"), gacc.host("accept")
+            assert np.array_equal(am, host(am0)) and np.array_equal(lg, host(lg0))
             a, bonus = oracle.verify(picks, d)
-            assert tuple(int(v) for v in host(acc)) == (a, bonus), (d, host(acc), (a, bonus))
+            assert tuple(int(v) for v in acc) == (a, bonus), (d, acc, (a, bonus))

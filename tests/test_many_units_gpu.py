@@ -9,7 +9,7 @@ import pytest
 
 import oracle
 import synth
-from gpu_util import check, dev, host, variant
+from gpu_util import Guarded, argmax_ok, check, dev, host, variant
 
 pytestmark = pytest.mark.gpu
 
@@ -42,9 +42,12 @@ def test_nvfp4_many_units_per_cta(sk, max_ctas, M, var, K, N):
     x = synth.x_f16(M, K, seed=K + M)
     codes, scales, g = synth.nvfp4_weights(N, K, seed=N + 1)
     y_ref, l1 = oracle.nvfp4_linear(x, codes, scales, g)
+    import torch
+
+    out = Guarded((M, N), torch.float32)
     with variant(sk, var):
-        y = host(sk.nvfp4_gemm(dev(x), dev(codes), dev(scales), float(g)))
-    check(y, y_ref, l1, False, f"nvfp4 ctas={max_ctas} M{M} K{K} N{N}")
+        sk.nvfp4_gemm(dev(x), dev(codes), dev(scales), float(g), y=out.t)
+    check(out.host("nvfp4 output"), y_ref, l1, False, f"nvfp4 ctas={max_ctas} M{M} K{K} N{N}")
 
 
 @pytest.mark.parametrize("M,var", MV)
@@ -53,9 +56,12 @@ def test_fp8_many_units_per_cta(sk, max_ctas, M, var, K, N):
     x = synth.x_f16(M, K, seed=K + M + 5)
     codes, scales = synth.fp8_weights(N, K, seed=N + 2)
     y_ref, l1 = oracle.fp8_linear(x, codes, scales)
+    import torch
+
+    out = Guarded((M, N), torch.float16)
     with variant(sk, var):
-        y = host(sk.fp8_gemm(dev(x), dev(codes), dev(scales), f16_out=True))
-    check(y, y_ref, l1, True, f"fp8 ctas={max_ctas} M{M} K{K} N{N}")
+        sk.fp8_gemm(dev(x), dev(codes), dev(scales), y=out.t, f16_out=True)
+    check(out.host("fp8 output"), y_ref, l1, True, f"fp8 ctas={max_ctas} M{M} K{K} N{N}")
 
 
 @pytest.mark.parametrize("M,var", [(1, "simt"), (1, "tensor"), (8, "auto")])
@@ -64,13 +70,14 @@ def test_lm_head_many_units_per_cta(sk, max_ctas, M, var):
     x = synth.x_f16(M, K, seed=77 + M)
     codes, scales, g = synth.nvfp4_weights(N, K, seed=78)
     y_ref, l1 = oracle.nvfp4_linear(x, codes, scales, g)
+    import torch
+
+    glg, gam = Guarded((M, N), torch.float32), Guarded((M,), torch.int32, fill=-7)
     with variant(sk, var):
-        logits, am = sk.lm_head_argmax(dev(x), dev(codes), dev(scales), float(g))
-    lg = host(logits)
+        sk.lm_head_argmax(dev(x), dev(codes), dev(scales), float(g), logits=glg.t, argmax=gam.t)
+    lg, am = glg.host("logits"), gam.host("argmax")
     check(lg, y_ref, l1, False, "lm_head few CTAs")
-    am = host(am)
-    for m in range(M):
-        assert am[m] == int(np.argmax(lg[m]))
+    argmax_ok(am, y_ref, l1, lg)
 
 
 def test_results_do_not_depend_on_grid(sk):

@@ -10,7 +10,7 @@ import pytest
 
 import oracle
 import synth
-from gpu_util import check, dev, host, variant
+from gpu_util import Guarded, check, dev, host, variant
 
 pytestmark = pytest.mark.gpu
 
@@ -27,12 +27,24 @@ def sk():
     assert skm.last_device_error() == skm.SK_OK
 
 
+def _out(M, N, f16):
+    import torch
+
+    return Guarded((M, N), torch.float16 if f16 else torch.float32)
+
+
 def nv_run(sk, x, codes, scales, g, f16=False):
-    return host(sk.nvfp4_gemm(dev(x), dev(codes), dev(scales), float(g), f16_out=f16))
+    """nvfp4_gemm into an output between guard bands (checked after the call)."""
+    y = _out(x.shape[0], codes.shape[0], f16)
+    sk.nvfp4_gemm(dev(x), dev(codes), dev(scales), float(g), y=y.t, f16_out=f16)
+    return y.host("nvfp4_gemm output")
 
 
 def f8_run(sk, x, codes, scales, f16=False):
-    return host(sk.fp8_gemm(dev(x), dev(codes), dev(scales), f16_out=f16))
+    """fp8_gemm into an output between guard bands (checked after the call)."""
+    y = _out(x.shape[0], codes.shape[0], f16)
+    sk.fp8_gemm(dev(x), dev(codes), dev(scales), y=y.t, f16_out=f16)
+    return y.host("fp8_gemm output")
 
 
 # ------------------------------------------------------------ config C0 ---
