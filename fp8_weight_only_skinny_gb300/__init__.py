@@ -7,6 +7,13 @@ include/skinny.h for the contract of each call.
 from ._binding import (  # noqa: F401
     EXPORTS,
     LIB_PATH,
+    SK_ERR_CUDA,
+    SK_ERR_INVALID_ARG,
+    SK_ERR_MISALIGNED,
+    SK_ERR_NOT_INITIALIZED,
+    SK_ERR_TIMEOUT,
+    SK_ERR_UNSUPPORTED_SHAPE,
+    SK_ERR_WORKSPACE,
     SK_OK,
     STATUS,
     VARIANT_AUTO,

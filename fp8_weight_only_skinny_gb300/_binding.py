@@ -23,6 +23,8 @@ STATUS = {
     7: "SK_ERR_WORKSPACE",
 }
 SK_OK = 0
+SK_ERR_INVALID_ARG, SK_ERR_UNSUPPORTED_SHAPE, SK_ERR_MISALIGNED = 1, 2, 3
+SK_ERR_NOT_INITIALIZED, SK_ERR_CUDA, SK_ERR_TIMEOUT, SK_ERR_WORKSPACE = 4, 5, 6, 7
 
 
 class SkinnyError(RuntimeError):

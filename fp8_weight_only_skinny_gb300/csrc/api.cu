@@ -32,6 +32,14 @@ int g_pdl = 1;
 std::atomic<int> g_variant{SK_VARIANT_AUTO};
 std::atomic<int> g_inject_stall{0};
 
+// Streams whose latest launch of this library was a weight quantizer (a short
+// list: one entry per stream that quantizes; see internal.h).
+std::mutex g_wq_mu;
+constexpr int MAX_MARKED_STREAMS = 64;
+cudaStream_t g_wq_streams[MAX_MARKED_STREAMS];
+int g_wq_n = 0;
+bool g_wq_overflow = false;   // more streams than slots: no linear launch uses PDL until one clears
+
 sk_status resolve_encode() {
     if (g_encode) return SK_OK;
     void *fn = nullptr;
@@ -144,19 +152,22 @@ sk_status run(Kind kind, const void *x, const uint8_t *codes, const void *scales
         const size_t need = size_t(p.U) * sk::unit_partial_bytes(mp);
         if (sk::WS_PARTIAL_OFFSET + need > d->bytes) return SK_ERR_WORKSPACE;
     }
-    p.stall = g_inject_stall.exchange(0);
+    p.stall = sk::take_inject_stall();
+    // No programmatic dependent launch right after a quantizer on this stream:
+    // its codes and scales must be complete before this kernel reads weights.
+    const bool pdl = !sk::take_weights_written(s) && g_pdl != 0;
 
     CUtensorMap tm_codes, tm_scales;
     if (nv) {
         if (!encode_map(&tm_codes, codes, uint64_t(K) / 2, uint64_t(N), sk::Traits<sk::NVFP4>::CODE_BOX_X) ||
             !encode_map(&tm_scales, scales, uint64_t(K) / 16, uint64_t(N), sk::Traits<sk::NVFP4>::SCALE_BOX_X))
             return SK_ERR_CUDA;
-        if (sk::launch_nvfp4(mp, f16, am, tm_codes, tm_scales, p, grid, s, g_pdl != 0) != cudaSuccess)
+        if (sk::launch_nvfp4(mp, f16, am, tm_codes, tm_scales, p, grid, s, pdl) != cudaSuccess)
             return SK_ERR_CUDA;
     } else {
         if (!encode_map(&tm_codes, codes, uint64_t(K), uint64_t(N), sk::Traits<sk::FP8>::CODE_BOX_X))
             return SK_ERR_CUDA;
-        if (sk::launch_fp8(mp, f16, tm_codes, p, grid, s, g_pdl != 0) != cudaSuccess) return SK_ERR_CUDA;
+        if (sk::launch_fp8(mp, f16, tm_codes, p, grid, s, pdl) != cudaSuccess) return SK_ERR_CUDA;
     }
     return SK_OK;
 }
@@ -170,6 +181,26 @@ namespace sk {
 // for M = 1 the SIMT variant wins only when each CTA streams many units (FP8
 // gate_up 5120x34816 at 36 units per CTA, NVFP4 lm_head at 156), because its
 // per-unit arithmetic is lighter while its fix-up and start-up are not.
+int take_inject_stall() { return g_inject_stall.exchange(0); }
+
+void note_weights_written(cudaStream_t stream) {
+    std::lock_guard<std::mutex> lk(g_wq_mu);
+    for (int i = 0; i < g_wq_n; ++i)
+        if (g_wq_streams[i] == stream) return;
+    if (g_wq_n < MAX_MARKED_STREAMS) g_wq_streams[g_wq_n++] = stream;
+    else g_wq_overflow = true;
+}
+
+bool take_weights_written(cudaStream_t stream) {
+    std::lock_guard<std::mutex> lk(g_wq_mu);
+    for (int i = 0; i < g_wq_n; ++i)
+        if (g_wq_streams[i] == stream) {
+            g_wq_streams[i] = g_wq_streams[--g_wq_n];
+            return true;
+        }
+    return g_wq_overflow;
+}
+
 unsigned char *current_workspace() {
     DeviceState *d = current(nullptr);
     return d ? d->ws : nullptr;

@@ -18,6 +18,19 @@ cudaError_t launch_fp8(int mp, bool f16out, const CUtensorMap &tm_codes, const P
 // Bytes of workspace-resident partial sums one unit writes (16 rows x mp tokens).
 inline size_t unit_partial_bytes(int mp) { return size_t(16) * mp * 4; }
 
+// The failure-injection request of sk_inject_wait_timeout(): returns 1 once
+// (and clears it) if the next kernel launch should issue no weight copies.
+int take_inject_stall();
+
+// The quantizers write weights.  A linear kernel reads its weights before
+// griddepcontrol.wait (its producer streams them while the previous kernel on
+// the stream finishes), so the first linear launch on a stream after a
+// quantizer launch goes without programmatic dependent launch.  The
+// quantizers mark their stream; every linear launch takes (clears) the mark
+// and learns whether it was set.
+void note_weights_written(cudaStream_t stream);
+bool take_weights_written(cudaStream_t stream);
+
 // Workspace of the current device (null before sk_init on it).
 unsigned char *current_workspace();
 

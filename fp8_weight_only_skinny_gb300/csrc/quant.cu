@@ -181,7 +181,9 @@ sk_status fp8_quantize(const void *w, uint8_t *codes, float *scales, int N, int 
     if (grid.y > 65535u) return SK_ERR_UNSUPPORTED_SHAPE;
     fp8_quantize_kernel<<<grid, QT, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
         reinterpret_cast<const __half *>(w), N, K, codes, scales);
-    return cudaGetLastError() == cudaSuccess ? SK_OK : SK_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess) return SK_ERR_CUDA;
+    sk::note_weights_written(reinterpret_cast<cudaStream_t>(stream));
+    return SK_OK;
 }
 
 sk_status nvfp4_quantize(const void *w, uint8_t *codes, uint8_t *scales, float *gscale, int N, int K,
@@ -205,7 +207,9 @@ sk_status nvfp4_quantize(const void *w, uint8_t *codes, uint8_t *scales, float *
     if (grid > 0x7FFFFFFFLL) return SK_ERR_UNSUPPORTED_SHAPE;
     nvfp4_quantize_kernel<<<unsigned(grid), QT, 0, s>>>(reinterpret_cast<const __half *>(w), nblocks, amax, codes,
                                                         scales, gscale);
-    return cudaGetLastError() == cudaSuccess ? SK_OK : SK_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess) return SK_ERR_CUDA;
+    sk::note_weights_written(s);
+    return SK_OK;
 }
 
 }  // extern "C"

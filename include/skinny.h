@@ -50,11 +50,19 @@
  *     another kernel that occupies SMs at the same time can make those waits
  *     run out (SK_ERR_TIMEOUT) instead of finishing.
  *     Consecutive calls on one stream may overlap through programmatic
- *     dependent launch: a kernel may start streaming its own weights while the
- *     previous kernel of this library finishes, but touches x, y and the
- *     workspace only after that kernel has completed.  So weights must not be
- *     written by the kernel immediately preceding the call on the same stream
- *     if that kernel is one of this library's (none of them writes weights).
+ *     dependent launch (PDL): a linear kernel may start streaming its own
+ *     weights while the kernel before it on the stream finishes, but touches
+ *     x, y and the workspace only after that kernel has completed.  Weights
+ *     are therefore read before the preceding kernel is known to be done:
+ *       * the library's own weight writers, fp8_quantize and nvfp4_quantize,
+ *         mark their stream, and the next linear call on that stream is
+ *         launched without PDL, so quantize-then-multiply on one stream is
+ *         safe with no synchronisation in between;
+ *       * a kernel from outside the library that writes the weights must not
+ *         be the kernel immediately preceding a linear call on the same
+ *         stream while PDL is on (sk_set_pdl(0) turns it off); anything
+ *         launched in between without PDL -- any other kernel, a copy, an
+ *         event wait -- ends the hazard.
  *   - Kernels bound every wait they spin on (about one second).  When a wait
  *     runs out the kernel records SK_ERR_TIMEOUT in a device word, finishes
  *     without further waiting and leaves garbage in y; sk_last_device_error()
@@ -283,15 +291,23 @@ SK_API void sk_inject_wait_timeout(int enable);
  * cudaFree, no library allocation) and needs no sk_init().
  *   Arguments, layouts and results are those of nvfp4_gemm (FP32 output).
  *   SK_ERR_WORKSPACE: the split-K partial sums of this shape do not fit the
- *   array (with K > 1024 they need ceil(N/16) * ceil(K/1024) * 64 * m bytes,
- *   m = 1, 2, 4 or 8 for M = 1, 2, 3..4, 5..8, at most about 7 MiB).
+ *   array.  With K > 1024 a call needs
+ *       ceil(N/16) * ceil(K/1024) * 64 * m  bytes  <=  7,335,936 bytes,
+ *   where m is the token slots of the kernel variant that runs: m = 8 for
+ *   every M >= 2, and for M = 1 unless the single-token variant is chosen
+ *   (sk_set_variant(SK_VARIANT_SIMT), or SK_VARIANT_AUTO on a shape with at
+ *   least 96 units of 16 rows x 1024 k per CTA), where m = 1.  For example
+ *   at M = 2 and K = 5120, N <= 45,840 fits and N = 45,856 is rejected.
+ *   K <= 1024 needs no partial sums.
  *   The first call on a device (with that device current) looks up the
  *   array's device address (cudaGetSymbolAddress), the tensor-map encoder and
  *   the SM count: make it before any stream capture.  All calls share the one
  *   array and leave their partial sums in it; each call clears the counters it
  *   needs before its kernel runs.  Calls whose kernels overlap on the GPU
  *   (different streams or host threads) race on the array.  Bounded-wait
- *   timeouts of this entry point are not reported by sk_last_device_error().
+ *   timeouts of this entry point are not reported by sk_last_device_error();
+ *   the next call starts from a cleared control block and counters, so it is
+ *   correct again.
  */
 SK_API sk_status nvfp4_gemm_noalloc(const void *x, const uint8_t *W_codes, const uint8_t *W_scales,
                                     float W_gscale, float *y, int M, int N, int K, void *stream);

@@ -163,3 +163,41 @@ def test_quantized_weights_feed_the_linears(sk, M):
     scale = np.abs(x.astype(np.float64)) @ np.abs(w.astype(np.float64)).T
     assert np.all(np.abs(y - exact) <= 0.2 * scale)          # 4-bit weights: coarse, but close
     assert np.all(np.abs(y8 - exact) <= 0.07 * scale)        # 8-bit weights: closer
+
+
+@pytest.mark.parametrize("M", [1, 8])
+def test_quantize_then_multiply_on_one_stream(sk, M):
+    """fp8_quantize rewrites the codes and scales and fp8_gemm reads them
+    right after it on the same stream, with programmatic dependent launch on
+    and no synchronisation in between: each product must use the weights just
+    written (a linear kernel streams weights before its dependency wait, so the
+    library launches the first linear call after a quantizer without PDL).
+    Three rounds alternate two weight matrices in the same buffers."""
+    import torch
+
+    N, K = 4096, 5120
+    ws = [_weights(N, K, seed, "normal") for seed in (61, 62)]
+    refs = []
+    x = synth.x_f16(M, K, seed=63)
+    for w in ws:
+        c, s = oracle.quantize_fp8(w)
+        refs.append(oracle.fp8_linear(x, c, s))
+    wd = [dev(w) for w in ws]
+    xd = dev(x)
+    codes = torch.empty((N, K), dtype=torch.uint8, device="cuda:0")
+    scales = torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device="cuda:0")
+    ys = [torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda:0") for _ in range(3)]
+    prev = sk.set_pdl(True)
+    try:
+        s = torch.cuda.Stream()
+        sp = s.cuda_stream
+        for r in range(3):
+            assert sk.lib.fp8_quantize(wd[r % 2].data_ptr(), codes.data_ptr(), scales.data_ptr(), N, K, sp) == 0
+            assert sk.lib.fp8_gemm(xd.data_ptr(), codes.data_ptr(), scales.data_ptr(), ys[r].data_ptr(),
+                                   M, N, K, sp) == 0
+        s.synchronize()
+    finally:
+        sk.set_pdl(prev)
+    for r in range(3):
+        y_ref, l1 = refs[r % 2]
+        check(host(ys[r]), y_ref, l1, False, f"fp8 gemm right after quantize, round {r}")
