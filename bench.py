@@ -157,6 +157,19 @@ class Linear:
         self.y = torch.empty((M, N), dtype=torch.float16 if out_f16 else torch.float32, device=dev)
         self.bytes = weight_bytes(fmt, K, N)
 
+    def at_m(self, M, gen, dev):
+        """The same weights with M activation rows of its own (another step
+        shape over the weights already in device memory)."""
+        import copy
+
+        import torch
+
+        o = copy.copy(self)
+        o.M = M
+        o.x = torch.randn((M, self.K), generator=gen, device=dev).to(torch.float16)
+        o.y = torch.empty((M, self.N), dtype=self.y.dtype, device=dev)
+        return o
+
     def call(self, sk, x=None):
         x = self.x if x is None else x
         if self.fmt == "nvfp4":
@@ -177,6 +190,15 @@ class LMHead(Linear):
         self.draft = torch.randint(0, LM_HEAD[3], (max(M - 1, 1),), generator=gen, device=dev,
                                    dtype=torch.int32)
         self.accept = torch.empty((2,), dtype=torch.int32, device=dev)
+
+    def at_m(self, M, gen, dev):
+        import torch
+
+        o = super().at_m(M, gen, dev)
+        o.am = torch.empty((M,), dtype=torch.int32, device=dev)
+        o.draft = torch.randint(0, LM_HEAD[3], (max(M - 1, 1),), generator=gen, device=dev, dtype=torch.int32)
+        o.accept = torch.empty((2,), dtype=torch.int32, device=dev)
+        return o
 
     def call(self, sk, x=None):
         x = self.x if x is None else x
@@ -431,74 +453,39 @@ def config(M):
             "parallelism": "replicas"}
 
 
-def run_ours(args):
+def time_stack(sk, calls, head, M, stream, steps, warmup, barrier=None, dist=None, clocks_index=None):
+    """The decode-round step: `calls` (64 layers x 4 linears + the lm_head)
+    captured once into a CUDA graph and replayed `steps` times, CUDA events on
+    the capture stream.  Then the same step end to end through the C ABI: the
+    activations (and the verify round's drafted tokens) copied from pinned host
+    memory and the picks (and the round's verdict) read back every step, all
+    inside the timed graph.  Returns a dict of the rates and the clock record."""
     import torch
 
-    import fp8_weight_only_skinny_gb300 as sk
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.init_process_group("nccl", device_id=dev)
-    barrier = (lambda: dist.barrier()) if dist else None
-    sk.init()
-    M = args.m
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(1234 + rank)
-    stream = torch.cuda.Stream(device=dev)
-    if args.layers_only:
-        peak, _ = peaks()
-        for tp in (False, True):
-            for r in layer_table(sk, gen, dev, stream, peak, tp=tp):
-                print(f"{'tp4 ' if tp else ''}{r['layer']:8s} {r['fmt']:5s} M={r['M']}  K={r['K']:6d} N={r['N']:6d} "
-                      f"{r['us']:8.2f} us  {r['GB/s']:8.1f} GB/s  {r['frac_of_peak'] * 100:5.1f}% of peak", flush=True)
-        for r in quant_rates(sk, gen, dev, stream, peak):
-            print(f"{r['op']:15s} K={r['K']} N={r['N']}  {r['us']:8.2f} us  {r['GB/s']:8.1f} GB/s  "
-                  f"{r['frac_of_peak'] * 100:5.1f}% of peak", flush=True)
-        print("lm_head greedy vs sampled:", sampler_cost(sk, gen, dev, stream), flush=True)
-        return
-
-    # ---- the decode-round stack
-    lins = []
-    for _ in range(N_LAYERS):
-        for name, f, K, N in LAYER:
-            lins.append(Linear(name, f, K, N, M, gen, dev))
-    head = LMHead(M, gen, dev)
-    calls = lins + [head]
-    assert sum(c.bytes for c in calls) == STEP_BYTES
+    dev = head.x.device
     graph = capture(lambda: [c.call(sk) for c in calls], stream)
-    launches_per_step = len(calls)
-
     with torch.cuda.stream(stream):          # replay() launches on the current stream
-        for _ in range(max(3, args.warmup)):
+        for _ in range(max(3, warmup)):
             graph.replay()
         stream.synchronize()
         if barrier:
             barrier()
-        with ClockSampler(local) as clk:
+        with ClockSampler(clocks_index if clocks_index is not None else dev.index) as clk:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            for _ in range(args.steps):
+            for _ in range(steps):
                 graph.replay()
             e1.record(stream)
             e1.synchronize()
             torch.cuda.synchronize()
             if barrier:
                 barrier()
-    value, ms = aggregate(e0.elapsed_time(e1) / args.steps, STEP_BYTES, dist)
+    value, ms = aggregate(e0.elapsed_time(e1) / steps, STEP_BYTES, dist)
+    del graph
     st = sk.last_device_error(stream)
     if st != 0:
         raise RuntimeError(f"device error {st}")
 
-    # ---- end to end through the C ABI: activations (and the drafted tokens of
-    # the verify round) from pinned host memory, the picks (and the round's
-    # verdict) back to the host, every step
     x_dev = torch.empty(sum(c.x.numel() for c in calls), dtype=torch.float16, device=dev)
     views, off = [], 0
     for c in calls:
@@ -545,12 +532,86 @@ def run_ours(args):
         cur.wait_stream(side)
 
     g2 = capture(e2e_step, stream)
-    e2e_value, e2e_ms = aggregate(time_graph(g2, stream, reps=args.steps, warmup=3, barrier=barrier),
-                                  STEP_BYTES, dist)
-    del g2
+    e2e_value, e2e_ms = aggregate(time_graph(g2, stream, reps=steps, warmup=3, barrier=barrier), STEP_BYTES, dist)
+    del g2, x_dev
+    return {"value": value, "ms": ms, "clocks": clk.summary(),
+            "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": int(h2d_bytes),
+                    "d2h_bytes_per_step": int(d2h_bytes), "ms_per_step": round(e2e_ms, 4)}}
+
+
+def c0_rate(sk, gen, dev, stream, peak, reps=64):
+    """The small GEMV case (NVFP4, M=1, K=512, N=256: 73,732 weight bytes).
+    Its weights stay in L2, so this is a latency figure, not a bandwidth one:
+    a graph of `reps` back-to-back launches on the same weights."""
+    K, N = 512, 256
+    lin = Linear("c0", "nvfp4", K, N, 1, gen, dev, out_f16=False)
+    g = capture(lambda: [lin.call(sk) for _ in range(reps)], stream)
+    ms = time_graph(g, stream, reps=10, warmup=3) / reps
+    b = weight_bytes("nvfp4", K, N)
+    gbs = b / (ms * 1e-3) / 1e9
+    return {"K": K, "N": N, "M": 1, "bytes": b, "us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
+            "frac_of_peak": round(gbs / peak, 4), "l2": "weights L2-resident (same weights every launch)"}
+
+
+def run_ours(args):
+    import torch
+
+    import fp8_weight_only_skinny_gb300 as sk
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    barrier = (lambda: dist.barrier()) if dist else None
+    sk.init()
+    M = args.m
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234 + rank)
+    stream = torch.cuda.Stream(device=dev)
+    if args.layers_only:
+        peak, _ = peaks()
+        for tp in (False, True):
+            for r in layer_table(sk, gen, dev, stream, peak, tp=tp):
+                print(f"{'tp4 ' if tp else ''}{r['layer']:8s} {r['fmt']:5s} M={r['M']}  K={r['K']:6d} N={r['N']:6d} "
+                      f"{r['us']:8.2f} us  {r['GB/s']:8.1f} GB/s  {r['frac_of_peak'] * 100:5.1f}% of peak", flush=True)
+        for r in quant_rates(sk, gen, dev, stream, peak):
+            print(f"{r['op']:15s} K={r['K']} N={r['N']}  {r['us']:8.2f} us  {r['GB/s']:8.1f} GB/s  "
+                  f"{r['frac_of_peak'] * 100:5.1f}% of peak", flush=True)
+        print("lm_head greedy vs sampled:", sampler_cost(sk, gen, dev, stream), flush=True)
+        return
+
+    # ---- the decode-round stack, and the same step end to end
+    lins = []
+    for _ in range(N_LAYERS):
+        for name, f, K, N in LAYER:
+            lins.append(Linear(name, f, K, N, M, gen, dev))
+    head = LMHead(M, gen, dev)
+    calls = lins + [head]
+    assert sum(c.bytes for c in calls) == STEP_BYTES
+    launches_per_step = len(calls)
+    main = time_stack(sk, calls, head, M, stream, args.steps, args.warmup, barrier, dist, clocks_index=local)
+
+    # ---- the other step shape over the same weights (single-GPU runs): the
+    # plain decode step at M = 1 next to the verify round, or the reverse
+    other = None
+    if world == 1 and not args.no_other_m:
+        Mo = 1 if M != 1 else 8
+        ocalls = [c.at_m(Mo, gen, dev) for c in calls]
+        r = time_stack(sk, ocalls, ocalls[-1], Mo, stream, args.steps, args.warmup, clocks_index=local)
+        other = {"M": Mo, "value": round(r["value"], 1), "unit": "GB/s", "ms_per_step": round(r["ms"], 4),
+                 "frac_of_peak": None, "e2e": r["e2e"], "clocks": r["clocks"]}
+        del ocalls
 
     # ---- dominant kernel alone (NVFP4 gate_up launch at this M), cold L2
     peak, peak_kind = peaks()
+    if other:
+        other["frac_of_peak"] = round(other["value"] / peak, 4)
     gu_ms, gu_bytes = cold_layer_rate(sk, "nvfp4", 5120, 34816, M, gen, dev, stream, copies=8)
     achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
     traffic = read_traffic(M)
@@ -558,21 +619,22 @@ def run_ours(args):
     # ---- per-layer tables, cold L2, M = 1 and 8: the full shapes, and the
     # per-rank shapes of 4-way tensor parallelism (the pages' own workload);
     # single-GPU runs only (every replica would measure the same)
-    layers, tp_layers, quant, sampler = [], [], [], None
+    layers, tp_layers, quant, sampler, c0 = [], [], [], None, None
+    del calls, lins, head
+    torch.cuda.empty_cache()
+    if world == 1:
+        c0 = c0_rate(sk, gen, dev, stream, peak)
     if not args.no_layers and world == 1:
         layers = layer_table(sk, gen, dev, stream, peak)
         tp_layers = layer_table(sk, gen, dev, stream, peak, tp=True)
         quant = quant_rates(sk, gen, dev, stream, peak)
         sampler = sampler_cost(sk, gen, dev, stream)
 
-    del graph, calls, lins, head
-    torch.cuda.empty_cache()
-
     if rank == 0:
         line = {
             "metric": "effective weight GB/s (decode-round linears, NVFP4+FP8)",
-            "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+            "value": round(main["value"], 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(main["ms"], 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f16 x {e2m1,e4m3} -> f32 accumulate",
             "data": "synthetic (device-generated weights, seeded)", "config": config(M),
             "roofline": {"bound": "hbm", "kernel": f"nvfp4 gate_up 5120x34816 M={M}, cold L2",
@@ -580,23 +642,34 @@ def run_ours(args):
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs)" if peak_kind == "measured"
                          else "fallback 6.8 TB/s"},
-            "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
-                    "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(d2h_bytes),
-                    "ms_per_step": round(e2e_ms, 4)},
+            "e2e": main["e2e"],
             "gpu_launches": launches_per_step * args.steps,
-            "clocks": clk.summary(),
-            "frac_of_peak": round(value / world / peak, 4),
+            "clocks": main["clocks"],
+            "frac_of_peak": round(main["value"] / world / peak, 4),
+            f"stack_m{other['M']}" if other else "stack_other_m": other,
+            "c0": c0,
             "layers": layers,
             "tp4_layers": tp_layers,
             "quantizers": quant,
             "lm_head_sampler": sampler,
         }
         if not args.no_cpu and world == 1:
+            import oracle
+
             gbs, cols, passes, dt, cores = cpu_oracle_sample(M)
             line["cpu_baseline"] = {
                 "value": round(gbs, 6), "unit": "GB/s", "cores": cores, "kind": "oracle",
                 "sample": f"{passes} pass(es) over {cols} output columns of each of qkv, o_proj, gate_up, "
                           f"down, lm_head at full K, M={M}, synthetic weights; {dt:.1f} s"}
+            oracle.set_threads(1)
+            try:
+                gbs1, cols1, passes1, dt1, _ = cpu_oracle_sample(M, budget_s=5.0)
+            finally:
+                oracle.set_threads(cores)
+            line["cpu_baseline_1thread"] = {
+                "value": round(gbs1, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": f"{passes1} pass(es) over {cols1} output columns of each of qkv, o_proj, gate_up, "
+                          f"down, lm_head at full K, M={M}, one thread; {dt1:.1f} s"}
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -673,6 +746,8 @@ def main():
     ap.add_argument("--m", type=int, default=8, choices=range(1, 9))
     ap.add_argument("--no-layers", action="store_true", help="skip the per-layer table")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-other-m", action="store_true",
+                    help="skip the second stack at the other step shape (M = 1 next to M > 1, or M = 8 next to M = 1)")
     ap.add_argument("--layers-only", action="store_true",
                     help="only print the per-layer cold-L2 table (development A/B runs)")
     ap.add_argument("--profile", metavar="LAYER:FMT",

@@ -17,6 +17,7 @@ from .oracle import (  # noqa: F401
     verify,
     tolerance,
     threads,
+    set_threads,
 )
 from .quant import e2m1_round, e4m3_round, quantize_fp8, quantize_nvfp4  # noqa: F401
 from .sample import margin as sample_margin, sample, sample_row  # noqa: F401

@@ -214,6 +214,18 @@ void oracle_verify(int64_t M, const int64_t *target, const int32_t *draft, int64
     accept[1] = target[a];
 }
 
+/* Threads for the column loops from now on (n >= 1); used to time the
+ * oracle single-threaded next to the OpenMP run.  Results do not depend on it. */
+void oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 int oracle_threads(void)
 {
 #ifdef _OPENMP

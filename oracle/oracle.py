@@ -58,6 +58,8 @@ def _load():
         lib.oracle_verify.restype = None
         lib.oracle_verify.argtypes = [i64, p, p, p]
         lib.oracle_threads.restype = ctypes.c_int
+        lib.oracle_set_threads.restype = None
+        lib.oracle_set_threads.argtypes = [ctypes.c_int]
         _lib = lib
     return _lib
 
@@ -69,6 +71,11 @@ def _ptr(a: np.ndarray):
 def threads() -> int:
     """OpenMP threads the oracle's column loop uses."""
     return int(_load().oracle_threads())
+
+
+def set_threads(n: int) -> None:
+    """Threads the column loops use from now on (the results do not depend on it)."""
+    _load().oracle_set_threads(int(n))
 
 
 def f16_to_f64(bits) -> np.ndarray:
