@@ -81,7 +81,9 @@ def test_noalloc_scratch_limit_boundary(sk, M):
     assert torch.isnan(y).all().item()                      # nothing ran
     st = _noalloc(sk, x, codes, scales, 1.0, y, M, N_in, K)
     assert st == sk.SK_OK, sk.status_string(st)
-    assert (host(y[:, :N_in]) == 0).all()
+    flat = host(y.view(-1))                                   # y is [M][N_in] row-major at this N
+    assert (flat[:M * N_in] == 0).all()
+    assert np.isnan(flat[M * N_in:]).all()
     assert sk.lib.nvfp4_gemm_noalloc(x.data_ptr(), codes.data_ptr(), scales.data_ptr(), 1.0, y.data_ptr(),
                                      9, 16, K, None) == sk.SK_ERR_INVALID_ARG
 
