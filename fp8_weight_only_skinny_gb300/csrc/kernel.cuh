@@ -49,7 +49,7 @@ constexpr int NGROUPS = 2;        // consumer groups per CTA
 constexpr int GROUP_THREADS = 128;
 constexpr int CTA_THREADS = NGROUPS * GROUP_THREADS + 32;   // + one producer warp
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;            // bounded waits: ~1 s
-constexpr int START_INFLIGHT = 3;   // copies outstanding per CTA during the first pass over the ring
+constexpr int START_INFLIGHT = 2;   // copies outstanding per CTA during the first pass over the ring
 // flags: [0] abort, [2] fix-up list length, [16 .. 16 + consumer threads) fix-up list
 constexpr int FLAG_BYTES = 64 + 4 * NGROUPS * GROUP_THREADS;
 
@@ -494,7 +494,8 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
                 // asks for its whole ring at once, HBM serves the burst in no
                 // particular order, some CTAs get their first tile microseconds
                 // after the others and finish last; pacing the first pass evens
-                // the start (measured: qkv FP8 M=8 9.7 -> 9.0 us per launch).
+                // the start (measured: qkv FP8 M=8 9.7 -> 9.0 us per launch with
+                // three copies in flight, 8.75 -> 8.49 us with two; one is slower).
                 if (i >= START_INFLIGHT && i < T::STAGES &&
                     !wait_bounded(bar_full + 8 * (i - START_INFLIGHT), 0, flags, &ctrl->err))
                     break;
