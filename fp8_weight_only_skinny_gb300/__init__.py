@@ -34,4 +34,5 @@ from ._binding import (  # noqa: F401
     set_variant,
     shutdown,
     status_string,
+    stream_workspace,
 )

@@ -42,6 +42,7 @@ def _load() -> ctypes.CDLL:
     sig = {
         "sk_init": ([ctypes.c_size_t], i),
         "sk_shutdown": ([], i),
+        "sk_stream_workspace": ([p, ctypes.c_size_t], i),
         "nvfp4_gemm": ([p, p, p, f, p, i, i, i, p], i),
         "nvfp4_gemm_f16out": ([p, p, p, f, p, i, i, i, p], i),
         "fp8_gemm": ([p, p, p, p, i, i, i, p], i),
@@ -69,7 +70,7 @@ def _load() -> ctypes.CDLL:
 lib = _load()
 
 # Names declared in include/skinny.h (the tests check that each is exported).
-EXPORTS = ("sk_init", "sk_shutdown", "nvfp4_gemm", "nvfp4_gemm_f16out", "fp8_gemm",
+EXPORTS = ("sk_init", "sk_shutdown", "sk_stream_workspace", "nvfp4_gemm", "nvfp4_gemm_f16out", "fp8_gemm",
            "fp8_gemm_f16out", "lm_head_argmax", "lm_head_verify", "lm_head_sample", "fp8_quantize",
            "nvfp4_quantize",
            "sk_status_string", "sk_last_device_error",
@@ -92,6 +93,12 @@ def init(workspace_bytes: int = 0) -> None:
 
 def shutdown() -> None:
     _check(lib.sk_shutdown(), "sk_shutdown")
+
+
+def stream_workspace(stream, workspace_bytes: int = 64 << 20) -> None:
+    """sk_stream_workspace: a workspace of its own for `stream` (a torch CUDA
+    stream) on the current device; 0 bytes removes it."""
+    _check(lib.sk_stream_workspace(_stream_ptr(stream), int(workspace_bytes)), "sk_stream_workspace")
 
 
 def set_pdl(enable: bool) -> bool:

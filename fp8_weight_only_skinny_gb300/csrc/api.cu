@@ -27,6 +27,16 @@ struct DeviceState {
 
 DeviceState g_dev[MAX_DEVICES];
 std::mutex g_mu;
+
+// Workspaces of individual streams (sk_stream_workspace), guarded by g_mu.
+struct StreamWs {
+    int dev = -1;
+    cudaStream_t stream = nullptr;
+    unsigned char *ws = nullptr;
+    size_t bytes = 0;
+};
+constexpr int MAX_STREAM_WS = 64;
+StreamWs g_sws[MAX_STREAM_WS];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 int g_pdl = 1;
 std::atomic<int> g_variant{SK_VARIANT_AUTO};
@@ -76,17 +86,39 @@ DeviceState *current(int *dev_out) {
     return d->ws ? d : nullptr;
 }
 
+// The workspace a call on `s` uses on the current device: the stream's own if
+// it has one (then `own` is set), else the device's; false if neither exists.
+struct WsRef {
+    unsigned char *ws = nullptr;
+    size_t bytes = 0;
+    int num_sms = 0;
+    bool own = false;
+};
+bool workspace_ref(cudaStream_t s, WsRef *r) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return false;
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (const StreamWs &e : g_sws)
+        if (e.ws && e.dev == dev && e.stream == s) {
+            *r = WsRef{e.ws, e.bytes, g_dev[dev].num_sms, true};
+            return true;
+        }
+    if (!g_dev[dev].ws) return false;
+    *r = WsRef{g_dev[dev].ws, g_dev[dev].bytes, g_dev[dev].num_sms, false};
+    return true;
+}
+
 // Persistent grid: CTAS_PER_SM CTAs per SM, never more CTAs than units.
 // SK_CTAS_PER_SM (1..4) overrides the CTAs per SM; SK_MAX_CTAS caps the grid,
 // which the tests use to give every CTA many units on small shapes (ring
 // wrap-around, k-chunk changes and multi-unit fix-ups).
-int grid_for(const DeviceState *d, long long units) {
+int grid_for(int num_sms, long long units) {
     int per_sm = 2;
     if (const char *e = std::getenv("SK_CTAS_PER_SM")) {
         const int v = std::atoi(e);
         if (v >= 1 && v <= 4) per_sm = v;
     }
-    long long g = (long long)(d->num_sms > 0 ? d->num_sms : 1) * per_sm;
+    long long g = (long long)(num_sms > 0 ? num_sms : 1) * per_sm;
     if (const char *e = std::getenv("SK_MAX_CTAS")) {
         const long long v = std::atoll(e);
         if (v >= 1 && v < g) g = v;
@@ -124,9 +156,9 @@ sk_status run(Kind kind, const void *x, const uint8_t *codes, const void *scales
         if (K == 0) return SK_ERR_UNSUPPORTED_SHAPE;   // no logits to verify against
         if (!aligned(accept, 4) || (draft && !aligned(draft, 4))) return SK_ERR_MISALIGNED;
     }
-    DeviceState *d = current(nullptr);
-    if (!d) return SK_ERR_NOT_INITIALIZED;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    WsRef wr;
+    if (!workspace_ref(s, &wr)) return SK_ERR_NOT_INITIALIZED;
     if (N == 0) return SK_OK;
     if (K == 0) return zero_outputs(y, size_t(M) * N * (f16 ? 2 : 4), argmax, M, s);
 
@@ -138,7 +170,7 @@ sk_status run(Kind kind, const void *x, const uint8_t *codes, const void *scales
     p.argmax = argmax;
     p.draft = draft;
     p.accept = accept;
-    p.ws = d->ws;
+    p.ws = wr.ws;
     p.M = M;
     p.N = N;
     p.K = K;
@@ -146,28 +178,33 @@ sk_status run(Kind kind, const void *x, const uint8_t *codes, const void *scales
     p.C = (K + sk::KC - 1) / sk::KC;
     p.KB = (K + 127) / 128;
     p.U = (long long)p.G * p.C;
-    const int grid = grid_for(d, p.U);
+    const int grid = grid_for(wr.num_sms, p.U);
     const int mp = sk::choose_mp(M, nv, p.U, grid);
     if (p.C > 1) {
         const size_t need = size_t(p.U) * sk::unit_partial_bytes(mp);
-        if (sk::WS_PARTIAL_OFFSET + need > d->bytes) return SK_ERR_WORKSPACE;
+        if (sk::WS_PARTIAL_OFFSET + need > wr.bytes) return SK_ERR_WORKSPACE;
     }
     p.stall = sk::take_inject_stall();
     // No programmatic dependent launch right after a quantizer on this stream:
     // its codes and scales must be complete before this kernel reads weights.
-    const bool pdl = !sk::take_weights_written(s) && g_pdl != 0;
+    // A stream with a workspace of its own may run beside other streams: its
+    // kernels launch cooperatively, so that the whole grid is resident before
+    // any CTA starts (the split-K owners wait on other CTAs of the grid), and
+    // without PDL.
+    const bool coop = wr.own;
+    const bool pdl = !sk::take_weights_written(s) && g_pdl != 0 && !coop;
 
     CUtensorMap tm_codes, tm_scales;
     if (nv) {
         if (!encode_map(&tm_codes, codes, uint64_t(K) / 2, uint64_t(N), sk::Traits<sk::NVFP4>::CODE_BOX_X) ||
             !encode_map(&tm_scales, scales, uint64_t(K) / 16, uint64_t(N), sk::Traits<sk::NVFP4>::SCALE_BOX_X))
             return SK_ERR_CUDA;
-        if (sk::launch_nvfp4(mp, f16, am, tm_codes, tm_scales, p, grid, s, pdl) != cudaSuccess)
+        if (sk::launch_nvfp4(mp, f16, am, tm_codes, tm_scales, p, grid, s, pdl, coop) != cudaSuccess)
             return SK_ERR_CUDA;
     } else {
         if (!encode_map(&tm_codes, codes, uint64_t(K), uint64_t(N), sk::Traits<sk::FP8>::CODE_BOX_X))
             return SK_ERR_CUDA;
-        if (sk::launch_fp8(mp, f16, tm_codes, p, grid, s, pdl) != cudaSuccess) return SK_ERR_CUDA;
+        if (sk::launch_fp8(mp, f16, tm_codes, p, grid, s, pdl, coop) != cudaSuccess) return SK_ERR_CUDA;
     }
     return SK_OK;
 }
@@ -201,9 +238,9 @@ bool take_weights_written(cudaStream_t stream) {
     return g_wq_overflow;
 }
 
-unsigned char *current_workspace() {
-    DeviceState *d = current(nullptr);
-    return d ? d->ws : nullptr;
+unsigned char *workspace_for(cudaStream_t stream) {
+    WsRef r;
+    return workspace_ref(stream, &r) ? r.ws : nullptr;
 }
 
 int choose_mp(int M, bool nvfp4, long long U, long long P) {
@@ -246,11 +283,53 @@ sk_status sk_init(size_t workspace_bytes) {
     return SK_OK;
 }
 
+sk_status sk_stream_workspace(void *stream, size_t workspace_bytes) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (resolve_encode() != SK_OK) return SK_ERR_CUDA;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return SK_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    StreamWs *slot = nullptr;
+    for (StreamWs &e : g_sws)
+        if (e.ws && e.dev == dev && e.stream == s) slot = &e;
+    if (slot) {
+        // Replace or remove: the stream's work must have finished with it.
+        if (cudaStreamSynchronize(s) != cudaSuccess) return SK_ERR_CUDA;
+        cudaFree(slot->ws);
+        *slot = StreamWs{};
+    }
+    if (workspace_bytes == 0) return SK_OK;
+    for (StreamWs &e : g_sws)
+        if (!e.ws) {
+            slot = &e;
+            break;
+        }
+    if (!slot) return SK_ERR_INVALID_ARG;   // MAX_STREAM_WS workspaces already
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SK_ERR_CUDA;
+    const size_t bytes = workspace_bytes < sk::WS_PARTIAL_OFFSET ? sk::WS_PARTIAL_OFFSET : workspace_bytes;
+    void *p = nullptr;
+    if (cudaMalloc(&p, bytes) != cudaSuccess) return SK_ERR_CUDA;
+    if (cudaMemset(p, 0, bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+        cudaFree(p);
+        return SK_ERR_CUDA;
+    }
+    g_dev[dev].num_sms = sms;
+    *slot = StreamWs{dev, s, static_cast<unsigned char *>(p), bytes};
+    return SK_OK;
+}
+
 sk_status sk_shutdown(void) {
     std::lock_guard<std::mutex> lk(g_mu);
     int prev = 0;
     cudaGetDevice(&prev);
     sk_status st = SK_OK;
+    for (StreamWs &e : g_sws) {
+        if (!e.ws) continue;
+        if (cudaSetDevice(e.dev) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) st = SK_ERR_CUDA;
+        cudaFree(e.ws);
+        e = StreamWs{};
+    }
     for (int i = 0; i < MAX_DEVICES; ++i) {
         if (!g_dev[i].ws) continue;
         if (cudaSetDevice(i) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) st = SK_ERR_CUDA;
@@ -310,10 +389,10 @@ const char *sk_status_string(sk_status status) {
 sk_status sk_last_device_error(void *stream) {
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (cudaStreamSynchronize(s) != cudaSuccess) return SK_ERR_CUDA;
-    DeviceState *d = current(nullptr);
-    if (!d) return SK_ERR_NOT_INITIALIZED;
+    WsRef wr;
+    if (!workspace_ref(s, &wr)) return SK_ERR_NOT_INITIALIZED;
     unsigned int err = 0;
-    unsigned char *word = d->ws + offsetof(sk::Ctrl, err);
+    unsigned char *word = wr.ws + offsetof(sk::Ctrl, err);
     if (cudaMemcpy(&err, word, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess) return SK_ERR_CUDA;
     if (err) {
         if (cudaMemset(word, 0, sizeof(err)) != cudaSuccess) return SK_ERR_CUDA;

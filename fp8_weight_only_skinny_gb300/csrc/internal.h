@@ -8,12 +8,13 @@ namespace sk {
 struct Params;
 
 // Launch one kernel of the given format.  mp: token slots of the variant
-// (1 = single-token SIMT variant; 8 = tensor-core variant).
+// (1 = single-token SIMT variant; 8 = tensor-core variant); pdl: programmatic
+// dependent launch; coop: cooperative launch (the whole grid co-resident).
 cudaError_t launch_nvfp4(int mp, bool f16out, bool argmax, const CUtensorMap &tm_codes,
                          const CUtensorMap &tm_scales, const Params &p, int grid,
-                         cudaStream_t stream, bool pdl);
+                         cudaStream_t stream, bool pdl, bool coop);
 cudaError_t launch_fp8(int mp, bool f16out, const CUtensorMap &tm_codes, const Params &p, int grid,
-                       cudaStream_t stream, bool pdl);
+                       cudaStream_t stream, bool pdl, bool coop);
 
 // Bytes of workspace-resident partial sums one unit writes (16 rows x mp tokens).
 inline size_t unit_partial_bytes(int mp) { return size_t(16) * mp * 4; }
@@ -31,8 +32,9 @@ int take_inject_stall();
 void note_weights_written(cudaStream_t stream);
 bool take_weights_written(cudaStream_t stream);
 
-// Workspace of the current device (null before sk_init on it).
-unsigned char *current_workspace();
+// The workspace a call on `stream` uses on the current device: the stream's
+// own (sk_stream_workspace), else the device's (sk_init); null if neither.
+unsigned char *workspace_for(cudaStream_t stream);
 
 // Token slots of the kernel variant for an M-token call of U units on a grid
 // of P CTAs: 1 (SIMT) or 8 (tensor-core), by the process-wide variant setting.

@@ -4,9 +4,9 @@
 namespace sk {
 
 cudaError_t launch_fp8(int mp, bool f16out, const CUtensorMap &tm_codes, const Params &p, int grid,
-                       cudaStream_t stream, bool pdl) {
-    if (f16out) return launch_by_m<FP8, true, false>(mp, tm_codes, tm_codes, p, grid, stream, pdl);
-    return launch_by_m<FP8, false, false>(mp, tm_codes, tm_codes, p, grid, stream, pdl);
+                       cudaStream_t stream, bool pdl, bool coop) {
+    if (f16out) return launch_by_m<FP8, true, false>(mp, tm_codes, tm_codes, p, grid, stream, pdl, coop);
+    return launch_by_m<FP8, false, false>(mp, tm_codes, tm_codes, p, grid, stream, pdl, coop);
 }
 
 }  // namespace sk

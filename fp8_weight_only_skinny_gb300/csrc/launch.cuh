@@ -7,9 +7,11 @@
 
 namespace sk {
 
+// pdl: programmatic dependent launch after the previous kernel on the stream;
+// coop: a cooperative launch (all CTAs co-resident before any starts).
 template <int FMT, int MP, bool F16OUT, bool ARGMAX>
 cudaError_t launch_variant(const CUtensorMap &tm_codes, const CUtensorMap &tm_scales, const Params &p,
-                           int grid, cudaStream_t stream, bool pdl) {
+                           int grid, cudaStream_t stream, bool pdl, bool coop) {
     auto kfn = skinny_kernel<FMT, MP, F16OUT, ARGMAX>;
     constexpr size_t smem = smem_bytes<FMT, MP>();
     static bool attr_done[64] = {};
@@ -26,19 +28,21 @@ cudaError_t launch_variant(const CUtensorMap &tm_codes, const CUtensorMap &tm_sc
     cfg.blockDim = dim3(CTA_THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = coop ? 1 : 0;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kfn, tm_codes, tm_scales, p);
 }
 
 template <int FMT, bool F16OUT, bool ARGMAX>
 cudaError_t launch_by_m(int mp, const CUtensorMap &tm_codes, const CUtensorMap &tm_scales,
-                        const Params &p, int grid, cudaStream_t stream, bool pdl) {
-    if (mp == 1) return launch_variant<FMT, 1, F16OUT, ARGMAX>(tm_codes, tm_scales, p, grid, stream, pdl);
-    return launch_variant<FMT, 8, F16OUT, ARGMAX>(tm_codes, tm_scales, p, grid, stream, pdl);
+                        const Params &p, int grid, cudaStream_t stream, bool pdl, bool coop) {
+    if (mp == 1) return launch_variant<FMT, 1, F16OUT, ARGMAX>(tm_codes, tm_scales, p, grid, stream, pdl, coop);
+    return launch_variant<FMT, 8, F16OUT, ARGMAX>(tm_codes, tm_scales, p, grid, stream, pdl, coop);
 }
 
 }  // namespace sk

@@ -142,7 +142,7 @@ sk_status nvfp4_gemm_noalloc(const void *x, const uint8_t *W_codes, const uint8_
         !na_encode_map(&tm_scales, W_scales, uint64_t(K) / 16, uint64_t(N), sk::Traits<sk::NVFP4>::SCALE_BOX_X))
         return SK_ERR_CUDA;
     sk::take_weights_written(s);   // launched without PDL anyway; clears a quantizer's mark
-    if (sk::launch_nvfp4(mp, false, false, tm_codes, tm_scales, p, grid, s, false) != cudaSuccess)
+    if (sk::launch_nvfp4(mp, false, false, tm_codes, tm_scales, p, grid, s, false, false) != cudaSuccess)
         return SK_ERR_CUDA;
     return SK_OK;
 }

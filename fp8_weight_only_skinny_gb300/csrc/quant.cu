@@ -192,9 +192,9 @@ sk_status nvfp4_quantize(const void *w, uint8_t *codes, uint8_t *scales, float *
     if (!w || !codes || !scales || !gscale) return SK_ERR_INVALID_ARG;
     if (K % 16) return SK_ERR_UNSUPPORTED_SHAPE;
     if (!aligned(w, 16) || !aligned(codes, 8) || !aligned(gscale, 4)) return SK_ERR_MISALIGNED;
-    unsigned char *ws = sk::current_workspace();
-    if (!ws) return SK_ERR_NOT_INITIALIZED;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    unsigned char *ws = sk::workspace_for(s);
+    if (!ws) return SK_ERR_NOT_INITIALIZED;
     unsigned int *amax = &reinterpret_cast<sk::Ctrl *>(ws)->qamax;
     const long long n8 = (long long)N * K / 8, nblocks = (long long)N * (K / 16);
     if (cudaMemsetAsync(amax, 0, sizeof(unsigned int), s) != cudaSuccess) return SK_ERR_CUDA;

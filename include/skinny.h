@@ -48,7 +48,10 @@
  *     kernel also expects its whole grid (two CTAs per SM) to be resident at
  *     once -- its split-K owners wait on the other CTAs of the grid -- so
  *     another kernel that occupies SMs at the same time can make those waits
- *     run out (SK_ERR_TIMEOUT) instead of finishing.
+ *     run out (SK_ERR_TIMEOUT) instead of finishing.  Streams that must run
+ *     at the same time each get a workspace of their own with
+ *     sk_stream_workspace(); their calls then launch cooperatively (the whole
+ *     grid resident before it starts), which rules both problems out.
  *     Consecutive calls on one stream may overlap through programmatic
  *     dependent launch (PDL): a linear kernel may start streaming its own
  *     weights while the kernel before it on the stream finishes, but touches
@@ -105,7 +108,27 @@ typedef enum {
  */
 SK_API sk_status sk_init(size_t workspace_bytes);
 
-/* Free the workspaces of all devices (synchronises each device first). */
+/*
+ * A workspace of its own for `stream` (a cudaStream_t; NULL = the legacy
+ * default stream) on the CURRENT device, allocated (cudaMalloc) and zeroed
+ * like sk_init's; workspace_bytes = 0 removes the stream's workspace (its calls
+ * fall back to the device's).  Calling it again replaces the workspace (after
+ * synchronising the stream).  Every later call on that stream -- linear
+ * layers, lm_head, quantizers, sk_last_device_error -- uses it instead of the
+ * device's, and its linear-layer kernels are launched cooperatively, so that
+ * the whole persistent grid is resident before any of its CTAs starts: calls
+ * on streams that each have a workspace of their own can then overlap on the
+ * GPU without racing on a workspace and without a split-K wait that could run
+ * out.  A cooperative kernel starts only when the whole grid fits, so
+ * overlapping calls share the SMs in turns rather than at once; such calls
+ * are also launched without programmatic dependent launch.  Up to 64 stream
+ * workspaces per process; more return SK_ERR_INVALID_ARG.  Call it before
+ * capturing a CUDA graph.  Needs no sk_init() (the device's workspace is
+ * only the fallback).
+ */
+SK_API sk_status sk_stream_workspace(void *stream, size_t workspace_bytes);
+
+/* Free the workspaces of all devices and streams (synchronises each device first). */
 SK_API sk_status sk_shutdown(void);
 
 /*
@@ -241,8 +264,9 @@ SK_API sk_status lm_head_sample(const void *x, const uint8_t *W_codes, const uin
 SK_API const char *sk_status_string(sk_status status);
 
 /*
- * Wait for `stream`, then read and clear the device error word of the current
- * device: SK_ERR_TIMEOUT if a kernel's bounded wait ran out since the last
+ * Wait for `stream`, then read and clear the device error word of the
+ * workspace that calls on `stream` use (the stream's own, else the current
+ * device's): SK_ERR_TIMEOUT if a kernel's bounded wait ran out since the last
  * call, SK_OK otherwise (SK_ERR_CUDA if the synchronisation itself failed).
  */
 SK_API sk_status sk_last_device_error(void *stream);
