@@ -49,7 +49,11 @@ constexpr int NGROUPS = 2;        // consumer groups per CTA
 constexpr int GROUP_THREADS = 128;
 constexpr int CTA_THREADS = NGROUPS * GROUP_THREADS + 32;   // + one producer warp
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;            // bounded waits: ~1 s
-constexpr int START_INFLIGHT = 2;   // copies outstanding per CTA during the first pass over the ring
+// Copies outstanding per CTA during the first pass over the ring: two for
+// short ranges (up to START_SHORT units per CTA), three otherwise.
+constexpr int START_INFLIGHT = 3;
+constexpr int START_INFLIGHT_SHORT = 2;
+constexpr int START_SHORT = 12;
 // flags: [0] abort, [2] fix-up list length, [16 .. 16 + consumer threads) fix-up list
 constexpr int FLAG_BYTES = 64 + 4 * NGROUPS * GROUP_THREADS;
 
@@ -101,7 +105,8 @@ template <> struct Traits<FP8> {
 static_assert(Traits<NVFP4>::STAGES % NGROUPS == 0, "ring stages must be a multiple of NGROUPS");
 static_assert(Traits<FP8>::STAGES % NGROUPS == 0, "ring stages must be a multiple of NGROUPS");
 static_assert(START_INFLIGHT >= 1 && START_INFLIGHT <= Traits<FP8>::STAGES &&
-                  START_INFLIGHT <= Traits<NVFP4>::STAGES,
+                  START_INFLIGHT <= Traits<NVFP4>::STAGES && START_INFLIGHT_SHORT >= 1 &&
+                  START_INFLIGHT_SHORT <= START_INFLIGHT,
               "start-up pacing must fit the ring");
 
 struct Params {
@@ -494,10 +499,12 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
                 // asks for its whole ring at once, HBM serves the burst in no
                 // particular order, some CTAs get their first tile microseconds
                 // after the others and finish last; pacing the first pass evens
-                // the start (measured: qkv FP8 M=8 9.7 -> 9.0 us per launch with
-                // three copies in flight, 8.75 -> 8.49 us with two; one is slower).
-                if (i >= START_INFLIGHT && i < T::STAGES &&
-                    !wait_bounded(bar_full + 8 * (i - START_INFLIGHT), 0, flags, &ctrl->err))
+                // the start (measured on the decode layers at M = 8: two copies
+                // in flight suit short ranges -- qkv FP8 8.75 -> 8.49 us per
+                // launch against three -- while long ranges do better with three
+                // -- NVFP4 gate_up 21.95 -> 21.53 us against two; one is slower).
+                const int si = n_units <= START_SHORT ? START_INFLIGHT_SHORT : START_INFLIGHT;
+                if (i >= si && i < T::STAGES && !wait_bounded(bar_full + 8 * (i - si), 0, flags, &ctrl->err))
                     break;
                 if (i >= T::STAGES &&
                     !wait_bounded(bar_empty + 8 * s, ((i / T::STAGES) & 1) ^ 1, flags, &ctrl->err))
