@@ -220,6 +220,33 @@ namespace sk {
 // per-unit arithmetic is lighter while its fix-up and start-up are not.
 int take_inject_stall() { return g_inject_stall.exchange(0); }
 
+bool encode_2d_u16(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                   uint32_t box_rows) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (resolve_encode() != SK_OK) return false;
+    }
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int device_sm_count() {
+    static int cached[MAX_DEVICES] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return 0;
+    if (cached[dev] == 0) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cached[dev] = sms;
+    }
+    return cached[dev];
+}
+
 void note_weights_written(cudaStream_t stream) {
     std::lock_guard<std::mutex> lk(g_wq_mu);
     for (int i = 0; i < g_wq_n; ++i)

@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <cstdint>
 
 namespace sk {
 
@@ -15,6 +16,15 @@ cudaError_t launch_nvfp4(int mp, bool f16out, bool argmax, const CUtensorMap &tm
                          cudaStream_t stream, bool pdl, bool coop);
 cudaError_t launch_fp8(int mp, bool f16out, const CUtensorMap &tm_codes, const Params &p, int grid,
                        cudaStream_t stream, bool pdl, bool coop);
+
+// 2-D TMA map over a row-major matrix of 16-bit elements [rows][cols]
+// (row stride cols * 2 bytes), box {box_cols, box_rows}, out-of-bounds reads
+// zero-filled.  Resolves the driver's encoder on first use; false on failure.
+bool encode_2d_u16(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                   uint32_t box_rows);
+
+// SM count of the current device (cached per device; 0 on failure).
+int device_sm_count();
 
 // Bytes of workspace-resident partial sums one unit writes (16 rows x mp tokens).
 inline size_t unit_partial_bytes(int mp) { return size_t(16) * mp * 4; }

@@ -70,40 +70,83 @@ __device__ __forceinline__ float block_max(float a, float *red) {
     return red[0];
 }
 
-// One CTA per 128 x 128 block: its absolute maximum, then its codes (the
-// second pass over the block's 32 KB is served by L2; keeping the block in
-// registers instead measured slower).
-__global__ void __launch_bounds__(QT) fp8_quantize_kernel(const __half *w, int N, int K, uint8_t *codes,
-                                                          float *scales) {
+// FP8: persistent CTAs, each streaming 128 x 128 blocks (b = blockIdx.x,
+// blockIdx.x + gridDim.x, ...) through two shared-memory buffers filled by 2-D
+// TMA loads (rows or columns past N or K are zero-filled, which leaves the
+// block maximum unchanged).  Each thread keeps its 64 halves of the block in
+// registers: their absolute maximum, the block maximum (two barriers), then
+// the codes from the same registers.  The block's buffer is refilled with the
+// block two ahead as soon as every thread has read it, so each CTA keeps two
+// blocks in flight and HBM is read once per weight.
+constexpr int FQ_BLK = 128;
+constexpr int FQ_BUF = FQ_BLK * FQ_BLK * 2;          // 32 KB of FP16
+constexpr size_t FQ_SMEM = 1024 + 2 * FQ_BUF + 16;
+constexpr uint64_t FQ_WAIT_NS = 1000000000ull;       // bounded waits: ~1 s
+
+__global__ void __launch_bounds__(QT) fp8_quantize_kernel(const __grid_constant__ CUtensorMap tm_w, int N, int K,
+                                                          int nbx, int nblocks, uint8_t *codes, float *scales) {
+    extern __shared__ unsigned char fq_smem[];
     __shared__ float red[QT / 32];
-    const int r0 = blockIdx.y * 128, c0 = blockIdx.x * 128;
-    const int rows = min(128, N - r0), cols = min(128, K - c0);
-    const int pieces = 128 * 16;   // 8 halves each
-    float a = 0.f;
-    for (int p = threadIdx.x; p < pieces; p += QT) {
-        const int r = p >> 4, cc = (p & 15) * 8;
-        if (r < rows && cc < cols) {
-            float f[8];
-            unpack8(*reinterpret_cast<const uint4 *>(w + size_t(r0 + r) * K + c0 + cc), f);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(f[i]));
-        }
+    const uint32_t raw = sk::smem_u32(fq_smem);
+    const uint32_t buf0 = (raw + 1023u) & ~1023u;
+    const uint32_t bar = buf0 + 2 * FQ_BUF;
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        sk::mbar_init(bar, 1);
+        sk::mbar_init(bar + 8, 1);
+        sk::fence_barrier_init();
     }
-    a = block_max(a, red);
-    const float s = a > 0.f ? __fdiv_rn(a, 448.f) : 1.f;
-    if (threadIdx.x == 0) scales[size_t(blockIdx.y) * gridDim.x + blockIdx.x] = s;
-    for (int p = threadIdx.x; p < pieces; p += QT) {
-        const int r = p >> 4, cc = (p & 15) * 8;
-        if (r < rows && cc < cols) {
+    __syncthreads();
+    auto issue = [&](int blk, int b) {
+        sk::mbar_arrive_expect_tx(bar + 8 * b, FQ_BUF);
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+            ::"r"(buf0 + b * FQ_BUF), "l"(reinterpret_cast<uint64_t>(&tm_w)), "r"((blk % nbx) * FQ_BLK),
+              "r"((blk / nbx) * FQ_BLK), "r"(bar + 8 * b)
+            : "memory");
+    };
+    if (tid == 0) {
+        if (int(blockIdx.x) < nblocks) issue(blockIdx.x, 0);
+        if (int(blockIdx.x + gridDim.x) < nblocks) issue(blockIdx.x + gridDim.x, 1);
+    }
+    int it = 0;
+    for (int blk = blockIdx.x; blk < nblocks; blk += gridDim.x, ++it) {
+        const int b = it & 1;
+        const uint64_t t0 = sk::globaltimer_ns();
+        while (!sk::mbar_try_wait(bar + 8 * b, (it >> 1) & 1)) {
+            if (sk::globaltimer_ns() - t0 > FQ_WAIT_NS) return;   // copy never landed: give up (codes unspecified)
+        }
+        // Thread tid holds words tid + 256 i of the block: row tid / 16 + 16 i,
+        // columns 8 (tid % 16) .. + 8 (a warp reads 512 contiguous bytes).
+        uint4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = sk::ld_shared_v4(buf0 + b * FQ_BUF + (tid + QT * i) * 16);
+        float a = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
             float f[8];
-            unpack8(*reinterpret_cast<const uint4 *>(w + size_t(r0 + r) * K + c0 + cc), f);
+            unpack8(v[i], f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(f[j]));
+        }
+        a = block_max(a, red);          // its barriers also order every read of the buffer
+        if (tid == 0 && blk + 2 * int(gridDim.x) < nblocks) issue(blk + 2 * gridDim.x, b);
+        const float s = a > 0.f ? __fdiv_rn(a, 448.f) : 1.f;
+        const int r0 = (blk / nbx) * FQ_BLK, c0 = (blk % nbx) * FQ_BLK;
+        if (tid == 0) scales[blk] = s;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = r0 + tid / 16 + 16 * i, cc = c0 + (tid % 16) * 8;
+            if (r >= N || cc >= K) continue;
+            float f[8];
+            unpack8(v[i], f);
             uint32_t lo = 0, hi = 0;
 #pragma unroll
-            for (int i = 0; i < 4; i += 2) {
-                lo |= e4m3x2_rn(__fdiv_rn(f[i], s), __fdiv_rn(f[i + 1], s)) << (8 * i);
-                hi |= e4m3x2_rn(__fdiv_rn(f[i + 4], s), __fdiv_rn(f[i + 5], s)) << (8 * i);
+            for (int j = 0; j < 4; j += 2) {
+                lo |= e4m3x2_rn(__fdiv_rn(f[j], s), __fdiv_rn(f[j + 1], s)) << (8 * j);
+                hi |= e4m3x2_rn(__fdiv_rn(f[j + 4], s), __fdiv_rn(f[j + 5], s)) << (8 * j);
             }
-            *reinterpret_cast<uint2 *>(codes + size_t(r0 + r) * K + c0 + cc) = make_uint2(lo, hi);
+            *reinterpret_cast<uint2 *>(codes + size_t(r) * K + cc) = make_uint2(lo, hi);
         }
     }
 }
@@ -177,10 +220,25 @@ sk_status fp8_quantize(const void *w, uint8_t *codes, float *scales, int N, int 
     if (!w || !codes || !scales) return SK_ERR_INVALID_ARG;
     if (K % 8) return SK_ERR_UNSUPPORTED_SHAPE;
     if (!aligned(w, 16) || !aligned(codes, 8) || !aligned(scales, 4)) return SK_ERR_MISALIGNED;
-    const dim3 grid((K + 127) / 128, (N + 127) / 128);
-    if (grid.y > 65535u) return SK_ERR_UNSUPPORTED_SHAPE;
-    fp8_quantize_kernel<<<grid, QT, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        reinterpret_cast<const __half *>(w), N, K, codes, scales);
+    const long long nbx = (K + 127) / 128, nby = (N + 127) / 128;
+    if (nbx * nby > 0x7FFFFFFFLL) return SK_ERR_UNSUPPORTED_SHAPE;
+    const int nblocks = int(nbx * nby);
+    CUtensorMap tm;
+    if (!sk::encode_2d_u16(&tm, w, uint64_t(K), uint64_t(N), FQ_BLK, FQ_BLK)) return SK_ERR_CUDA;
+    static bool attr_done[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SK_ERR_CUDA;
+    if (dev < 64 && !attr_done[dev]) {
+        if (cudaFuncSetAttribute(fp8_quantize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(FQ_SMEM)) !=
+            cudaSuccess)
+            return SK_ERR_CUDA;
+        attr_done[dev] = true;
+    }
+    const int sms = sk::device_sm_count();
+    const int cap = (sms > 0 ? sms : 1) * 3;                   // three CTAs (2 x 32 KB buffers) per SM
+    const int grid = nblocks < cap ? nblocks : cap;
+    fp8_quantize_kernel<<<grid, QT, FQ_SMEM, reinterpret_cast<cudaStream_t>(stream)>>>(tm, N, K, int(nbx), nblocks,
+                                                                                    codes, scales);
     if (cudaGetLastError() != cudaSuccess) return SK_ERR_CUDA;
     sk::note_weights_written(reinterpret_cast<cudaStream_t>(stream));
     return SK_OK;
