@@ -14,11 +14,16 @@ same distributions the tests use, and far larger than L2, so every replay
 streams them from HBM.  Metric: weight bytes (codes + scales + tensor scale)
 per second.
 
-Also measured: the dominant kernel alone (the NVFP4 gate_up launch, rotating
-over 8 weight copies = 802 MB so L2 is cold) for the roofline, a per-layer
-table with cold L2 at M = 1 and 8, and the end-to-end rate through the C ABI
-with the activations (and drafted tokens) copied from pinned host memory and
-the picks (and the round's verdict) read back every step.  --impl reference times the CPU oracle on a bounded sample.
+Also measured: the same step at the other token count over the same weights
+(M = 1 next to the verify round: `stack_m1`), the dominant kernel alone (the
+NVFP4 gate_up launch, rotating over 8 weight copies = 802 MB so L2 is cold) for
+the roofline, the small NVFP4 GEMV (K=512, N=256, L2-resident: `c0`), a
+per-layer table with cold L2 at M = 1 and 8 (full and 4-way tensor-parallel
+per-rank shapes), the quantizers and the sampled lm_head, and the end-to-end
+rate through the C ABI with the activations (and drafted tokens) copied from
+pinned host memory and the picks (and the round's verdict) read back every
+step.  The CPU oracle is timed on a bounded sample with all host threads and
+with one.  --impl reference times the CPU oracle on a bounded sample.
 """
 from __future__ import annotations
 
