@@ -29,10 +29,12 @@
 // Units are numbered chunk-major, u = c * G + g (G row groups, C k-chunks),
 // and CTA b takes the contiguous range [b*U/P, (b+1)*U/P), so every CTA
 // streams the same number of bytes (+-1 unit) whatever the shape.  Each unit
-// yields a 16 x MP partial sum; when C > 1 it goes to the workspace and the
-// CTA that delivers the last partial of a row group (an atomic counter per row
-// group) sums the C partials in ascending chunk order and writes y.  The sum
-// order is therefore fixed: results are bitwise reproducible.
+// yields a 16 x MP partial sum; when C > 1 it goes to the workspace, and once
+// all C partials of a row group are in (an atomic counter per row group) one
+// CTA sums them in ascending chunk order and writes y: the CTA that delivered
+// the last partial when every CTA holds few units, else the row group's
+// assigned owner.  The sum order is fixed either way: results are bitwise
+// reproducible.
 #pragma once
 #include <cuda.h>
 #include <cstdint>
@@ -54,6 +56,9 @@ constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;            // bounded waits: ~
 constexpr int START_INFLIGHT = 3;
 constexpr int START_INFLIGHT_SHORT = 2;
 constexpr int START_SHORT = 12;
+// The MMA variant sums split-K row groups by their last contributor when no CTA
+// holds more than this many units, by assigned owners otherwise.
+constexpr int LAST_MAX = 8;
 // flags: [0] abort, [2] fix-up list length, [16 .. 16 + consumer threads) fix-up list
 constexpr int FLAG_BYTES = 64 + 4 * NGROUPS * GROUP_THREADS;
 
@@ -589,31 +594,54 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
         named_bar_sync(bar_id, GROUP_THREADS);   // gred is reused by the next unit
     }
 
-    if (MP != 8 && p.C > 1) {
-        // Split-K fix-up, SIMT variants (few outputs per row group): one counter
-        // atomic per unit of this CTA, CT at a time; the CTA whose atomic
-        // completes a row group sums its C partials in ascending chunk order.
-        // CTAs that complete nothing leave at once.
+    // Split-K fix-up by the last contributor (the SIMT variants, and the MMA
+    // variant when no CTA holds more than LAST_MAX units): after a CTA barrier
+    // (which orders every thread's partial stores before it) one acquire-release
+    // counter increment per unit of this CTA, all in flight at once; the CTA
+    // whose increment completes a row group sums its C partials in ascending
+    // chunk order, and a CTA that completes nothing leaves at once.  With long
+    // ranges the last CTA to finish would complete most of its row groups and
+    // sum them alone, so those use the owner scheme below (measured at 8 units
+    // per CTA or fewer: the small decode layers 0.1-0.3 us and the 4-way
+    // tensor-parallel shards up to 0.4 us faster per launch; at 36 units
+    // (gate_up) 3.5 us slower).
+    if (p.C > 1 && (MP != 8 || p.U <= (long long)LAST_MAX * gridDim.x)) {
         int *fix_n = const_cast<int *>(flags) + 2;
         int *fix_list = const_cast<int *>(flags) + 16;          // CT entries
+        constexpr int ES = CT / NOUT;
+        const int o = ct % NOUT;
         for (int b0 = 0; b0 < n_units; b0 += CT) {
             if (ct == 0) *fix_n = 0;
             named_bar_sync(15, CT);
-            // Release: the barrier orders every thread's partial stores before
-            // this fence, and the fence orders them before this thread's atomic.
-            // Acquire: the same fence after the atomic, before the barrier that
-            // precedes every thread's partial loads.
             const int i = b0 + ct;
             if (i < n_units) {
                 const int g = int((u_lo + i) % p.G);
-                __threadfence();
-                if (atomicAdd(counters + g, 1u) == unsigned(p.C - 1)) fix_list[atomicAdd(fix_n, 1)] = g;
-                __threadfence();
+                if (atom_add_acq_rel_u32(counters + g, 1u) == unsigned(p.C - 1)) fix_list[atomicAdd(fix_n, 1)] = g;
             }
             named_bar_sync(15, CT);
+            // Thread ct sums output o of listed row groups e0, e0 + ES, ... (up
+            // to four at a time), with all their partials (up to eight chunks
+            // each) in flight before the additions; many chunks (down: 17): one
+            // row group at a time with up to 24 partials in flight.
             const int n_fix = *fix_n;
-            constexpr int ES = CT / NOUT;
-            const int o = ct % NOUT;
+            constexpr int CB = 8;
+            if (p.C > CB) {
+                constexpr int CL = 24;
+                for (int e = ct / NOUT; e < n_fix; e += ES) {
+                    const int gq = fix_list[e];
+                    float acc = 0.f;
+                    for (int c0 = 0; c0 < p.C; c0 += CL) {
+                        float v[CL];
+#pragma unroll
+                        for (int k = 0; k < CL; ++k)
+                            v[k] = c0 + k < p.C ? ld_cg_f32(partials + ((size_t)gq * p.C + c0 + k) * NOUT + o) : 0.f;
+#pragma unroll
+                        for (int k = 0; k < CL; ++k)
+                            if (c0 + k < p.C) acc += v[k];
+                    }
+                    finalize<FMT, MP, F16OUT, ARGMAX>(p, gq, o, acc, best);
+                }
+            } else
             for (int e = ct / NOUT; e < n_fix; e += 4 * ES) {
                 int gg[4];
                 float acc[4];
@@ -622,11 +650,20 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
                     gg[j] = e + j * ES < n_fix ? fix_list[e + j * ES] : -1;
                     acc[j] = 0.f;
                 }
-#pragma unroll 4
-                for (int cc = 0; cc < p.C; ++cc) {
+                for (int c0 = 0; c0 < p.C; c0 += CB) {
+                    float v[4][CB];
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        if (gg[j] >= 0) acc[j] += ld_cg_f32(partials + ((size_t)gg[j] * p.C + cc) * NOUT + o);
+#pragma unroll
+                        for (int k = 0; k < CB; ++k)
+                            v[j][k] = (gg[j] >= 0 && c0 + k < p.C)
+                                          ? ld_cg_f32(partials + ((size_t)gg[j] * p.C + c0 + k) * NOUT + o)
+                                          : 0.f;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+#pragma unroll
+                        for (int k = 0; k < CB; ++k)
+                            if (c0 + k < p.C) acc[j] += v[j][k];
                 }
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
@@ -635,11 +672,10 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
             if (ct < n_fix) counters[fix_list[ct]] = 0u;
             named_bar_sync(15, CT);
         }
-    }
-
-    if (MP == 8 && p.C > 1) {
-        // Split-K fix-up, MMA variant (128 outputs per row group: the sums are
-        // the heavy part, so they are shared out evenly).  (1) Publish: after a
+    } else if (MP == 8 && p.C > 1) {
+        // Split-K fix-up by owners, MMA variant with more than LAST_MAX units
+        // per CTA (128 outputs per row group: the sums are the heavy part, so
+        // they are shared out evenly).  (1) Publish: after a
         // CTA barrier (which orders every thread's partial stores before it),
         // fire-and-forget release reductions on the counters, one per unit of
         // this CTA (measured: the small FP8 layers ~2 % faster than a fence

@@ -190,6 +190,15 @@ __device__ __forceinline__ void red_release_add_u32(unsigned int *p, unsigned in
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Fetch-and-add at GPU scope with acquire-release semantics: releases the
+// stores ordered before it (a preceding CTA barrier makes them cumulative) and
+// acquires those released by earlier increments of the same counter.
+__device__ __forceinline__ unsigned int atom_add_acq_rel_u32(unsigned int *p, unsigned int v) {
+    unsigned int old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 // Bring the line holding `p` into L1 (no register, no wait).
 __device__ __forceinline__ void prefetch_l1(const void *p) {
     asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
