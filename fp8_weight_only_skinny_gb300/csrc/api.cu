@@ -146,7 +146,6 @@ sk_status run(Kind kind, const void *x, const uint8_t *codes, const void *scales
     if (!x || !codes || !scales) return SK_ERR_INVALID_ARG;
     if (am ? !argmax : !y) return SK_ERR_INVALID_ARG;
     if (nv ? (K % 256) : (K % 128)) return SK_ERR_UNSUPPORTED_SHAPE;
-    if (size_t(N) > sk::WS_MAX_ROWGROUPS * sk::RG) return SK_ERR_UNSUPPORTED_SHAPE;
     if (!aligned(x, 16) || !aligned(codes, 16)) return SK_ERR_MISALIGNED;
     if (nv ? !aligned(scales, 16) : !aligned(scales, 4)) return SK_ERR_MISALIGNED;
     if (y && !aligned(y, f16 ? 2 : 4)) return SK_ERR_MISALIGNED;
@@ -212,6 +211,20 @@ sk_status run(Kind kind, const void *x, const uint8_t *codes, const void *scales
 }  // namespace
 
 namespace sk {
+
+__global__ void fill_u32_kernel(unsigned int *p, size_t n, unsigned int v) {
+    for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += size_t(gridDim.x) * blockDim.x)
+        p[i] = v;
+}
+
+cudaError_t empty_partials(unsigned char *ws, size_t bytes, cudaStream_t stream) {
+    const size_t n = bytes / 4;
+    if (n == 0) return cudaSuccess;
+    const size_t blocks = (n + 255) / 256;
+    fill_u32_kernel<<<unsigned(blocks < 1024 ? blocks : 1024), 256, 0, stream>>>(
+        reinterpret_cast<unsigned int *>(ws + WS_PARTIAL_OFFSET), n, PARTIAL_EMPTY);
+    return cudaGetLastError();
+}
 
 // Measured on GB300 (cold L2, graphs of back-to-back launches): for M >= 2 the
 // tensor-core variant is faster on every decode-layer shape (up to 2x at M = 4);
@@ -300,7 +313,9 @@ sk_status sk_init(size_t workspace_bytes) {
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SK_ERR_CUDA;
     void *p = nullptr;
     if (cudaMalloc(&p, bytes) != cudaSuccess) return SK_ERR_CUDA;
-    if (cudaMemset(p, 0, bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+    if (cudaMemset(p, 0, sk::WS_CTRL_BYTES) != cudaSuccess ||
+        sk::empty_partials(static_cast<unsigned char *>(p), bytes - sk::WS_PARTIAL_OFFSET, 0) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
         cudaFree(p);
         return SK_ERR_CUDA;
     }
@@ -337,7 +352,9 @@ sk_status sk_stream_workspace(void *stream, size_t workspace_bytes) {
     const size_t bytes = workspace_bytes < sk::WS_PARTIAL_OFFSET ? sk::WS_PARTIAL_OFFSET : workspace_bytes;
     void *p = nullptr;
     if (cudaMalloc(&p, bytes) != cudaSuccess) return SK_ERR_CUDA;
-    if (cudaMemset(p, 0, bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+    if (cudaMemset(p, 0, sk::WS_CTRL_BYTES) != cudaSuccess ||
+        sk::empty_partials(static_cast<unsigned char *>(p), bytes - sk::WS_PARTIAL_OFFSET, 0) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
         cudaFree(p);
         return SK_ERR_CUDA;
     }

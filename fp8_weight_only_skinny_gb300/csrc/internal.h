@@ -26,6 +26,10 @@ bool encode_2d_u16(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows
 // SM count of the current device (cached per device; 0 on failure).
 int device_sm_count();
 
+// Mark the first `bytes` of the split-K partial slots of workspace `ws` empty
+// (every slot must be empty before a launch uses the workspace), on `stream`.
+cudaError_t empty_partials(unsigned char *ws, size_t bytes, cudaStream_t stream);
+
 // Bytes of workspace-resident partial sums one unit writes (16 rows x mp tokens).
 inline size_t unit_partial_bytes(int mp) { return size_t(16) * mp * 4; }
 

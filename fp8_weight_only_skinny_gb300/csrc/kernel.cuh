@@ -29,12 +29,10 @@
 // Units are numbered chunk-major, u = c * G + g (G row groups, C k-chunks),
 // and CTA b takes the contiguous range [b*U/P, (b+1)*U/P), so every CTA
 // streams the same number of bytes (+-1 unit) whatever the shape.  Each unit
-// yields a 16 x MP partial sum; when C > 1 it goes to the workspace, and once
-// all C partials of a row group are in (an atomic counter per row group) one
-// CTA sums them in ascending chunk order and writes y: the CTA that delivered
-// the last partial when every CTA holds few units, else the row group's
-// assigned owner.  The sum order is fixed either way: results are bitwise
-// reproducible.
+// yields a 16 x MP partial sum; when C > 1 it goes to a slot of its own in
+// the workspace, and the row group's owner CTA waits for its C slots to fill,
+// sums them in ascending chunk order and writes y.  The sum order is fixed:
+// results are bitwise reproducible.
 #pragma once
 #include <cuda.h>
 #include <cstdint>
@@ -56,16 +54,18 @@ constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;            // bounded waits: ~
 constexpr int START_INFLIGHT = 3;
 constexpr int START_INFLIGHT_SHORT = 2;
 constexpr int START_SHORT = 12;
-// The MMA variant sums split-K row groups by their last contributor when no CTA
-// holds more than this many units, by assigned owners otherwise.
-constexpr int LAST_MAX = 8;
-// flags: [0] abort, [2] fix-up list length, [16 .. 16 + consumer threads) fix-up list
-constexpr int FLAG_BYTES = 64 + 4 * NGROUPS * GROUP_THREADS;
+// An empty split-K partial slot: a signalling-NaN bit pattern, which FP32
+// arithmetic never produces (its NaN results are the canonical quiet NaN), so
+// a slot holding anything else holds a partial sum.  Every slot of a workspace
+// is empty between launches: the workspace is created filled with it, and an
+// owner empties each slot it has summed.
+constexpr unsigned int PARTIAL_EMPTY = 0x7FBADBADu;
+// flags: [0] abort
+constexpr int FLAG_BYTES = 64;
 
-// Workspace layout (bytes): control block, row-group counters, partial sums.
+// Workspace layout (bytes): control block, then the split-K partial slots.
 constexpr size_t WS_CTRL_BYTES = 4096;
-constexpr size_t WS_MAX_ROWGROUPS = size_t(1) << 18;
-constexpr size_t WS_PARTIAL_OFFSET = WS_CTRL_BYTES + WS_MAX_ROWGROUPS * 4;
+constexpr size_t WS_PARTIAL_OFFSET = WS_CTRL_BYTES;
 
 struct Ctrl {
     unsigned long long argmax_key[8];   // per token: (ordered logit << 32) | ~n
@@ -432,11 +432,10 @@ __device__ __forceinline__ void finalize(const Params &p, int g, int o, float v,
 // i % NGROUPS, whose four warps split its k-chunk or its rows); the last warp
 // is the producer, one lane of which issues the TMA loads.  Per unit a group
 // reduces its warps' partial sums through shared memory and either writes y
-// (one k-chunk) or stores the unit's split-K partial with a plain store.  The
-// counter atomics that find the last contributor of each row group, and the
-// sums of the C partials in ascending chunk order, run once per CTA after its
-// whole range, by all consumer threads in parallel: no global round trip sits
-// on the per-unit path.
+// (one k-chunk) or stores the unit's split-K partial into its slot.  The sums
+// of the C partials of each owned row group, in ascending chunk order, run
+// once per CTA after its whole range, by all consumer threads in parallel: no
+// global round trip sits on the per-unit path.
 template <int FMT, int MP, bool F16OUT, bool ARGMAX>
 __global__ void __launch_bounds__(CTA_THREADS, 2)
 skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
@@ -458,7 +457,6 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
         sb + T::STAGES * T::STAGE_BYTES + 16 * T::STAGES + NGROUPS * RED * 4 + FLAG_BYTES);
 
     Ctrl *ctrl = reinterpret_cast<Ctrl *>(p.ws);
-    unsigned int *counters = reinterpret_cast<unsigned int *>(p.ws + WS_CTRL_BYTES);
     float *partials = reinterpret_cast<float *>(p.ws + WS_PARTIAL_OFFSET);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -589,151 +587,73 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
             if constexpr (MP == 8) v = gred[t] + gred[128 + t] + gred[256 + t] + gred[384 + t];
             else v = gred[t];
             if (p.C == 1) finalize<FMT, MP, F16OUT, ARGMAX>(p, g, t, v, best);
-            else partials[((size_t)g * p.C + c) * NOUT + t] = v;   // plain store
+            else st_relaxed_f32(partials + ((size_t)g * p.C + c) * NOUT + t, v);
         }
         named_bar_sync(bar_id, GROUP_THREADS);   // gred is reused by the next unit
     }
 
-    // Split-K fix-up by the last contributor (the SIMT variants, and the MMA
-    // variant when no CTA holds more than LAST_MAX units): after a CTA barrier
-    // (which orders every thread's partial stores before it) one acquire-release
-    // counter increment per unit of this CTA, all in flight at once; the CTA
-    // whose increment completes a row group sums its C partials in ascending
-    // chunk order, and a CTA that completes nothing leaves at once.  With long
-    // ranges the last CTA to finish would complete most of its row groups and
-    // sum them alone, so those use the owner scheme below (measured at 8 units
-    // per CTA or fewer: the small decode layers 0.1-0.3 us and the 4-way
-    // tensor-parallel shards up to 0.4 us faster per launch; at 36 units
-    // (gate_up) 3.5 us slower).
-    if (p.C > 1 && (MP != 8 || p.U <= (long long)LAST_MAX * gridDim.x)) {
-        int *fix_n = const_cast<int *>(flags) + 2;
-        int *fix_list = const_cast<int *>(flags) + 16;          // CT entries
-        constexpr int ES = CT / NOUT;
-        const int o = ct % NOUT;
-        for (int b0 = 0; b0 < n_units; b0 += CT) {
-            if (ct == 0) *fix_n = 0;
-            named_bar_sync(15, CT);
-            const int i = b0 + ct;
-            if (i < n_units) {
-                const int g = int((u_lo + i) % p.G);
-                if (atom_add_acq_rel_u32(counters + g, 1u) == unsigned(p.C - 1)) fix_list[atomicAdd(fix_n, 1)] = g;
-            }
-            named_bar_sync(15, CT);
-            // Thread ct sums output o of listed row groups e0, e0 + ES, ... (up
-            // to four at a time), with all their partials (up to eight chunks
-            // each) in flight before the additions; many chunks (down: 17): one
-            // row group at a time with up to 24 partials in flight.
-            const int n_fix = *fix_n;
-            constexpr int CB = 8;
-            if (p.C > CB) {
-                constexpr int CL = 24;
-                for (int e = ct / NOUT; e < n_fix; e += ES) {
-                    const int gq = fix_list[e];
-                    float acc = 0.f;
-                    for (int c0 = 0; c0 < p.C; c0 += CL) {
-                        float v[CL];
-#pragma unroll
-                        for (int k = 0; k < CL; ++k)
-                            v[k] = c0 + k < p.C ? ld_cg_f32(partials + ((size_t)gq * p.C + c0 + k) * NOUT + o) : 0.f;
-#pragma unroll
-                        for (int k = 0; k < CL; ++k)
-                            if (c0 + k < p.C) acc += v[k];
-                    }
-                    finalize<FMT, MP, F16OUT, ARGMAX>(p, gq, o, acc, best);
-                }
-            } else
-            for (int e = ct / NOUT; e < n_fix; e += 4 * ES) {
-                int gg[4];
-                float acc[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    gg[j] = e + j * ES < n_fix ? fix_list[e + j * ES] : -1;
-                    acc[j] = 0.f;
-                }
-                for (int c0 = 0; c0 < p.C; c0 += CB) {
-                    float v[4][CB];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-#pragma unroll
-                        for (int k = 0; k < CB; ++k)
-                            v[j][k] = (gg[j] >= 0 && c0 + k < p.C)
-                                          ? ld_cg_f32(partials + ((size_t)gg[j] * p.C + c0 + k) * NOUT + o)
-                                          : 0.f;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-#pragma unroll
-                        for (int k = 0; k < CB; ++k)
-                            if (c0 + k < p.C) acc[j] += v[j][k];
-                }
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (gg[j] >= 0) finalize<FMT, MP, F16OUT, ARGMAX>(p, gg[j], o, acc[j], best);
-            }
-            if (ct < n_fix) counters[fix_list[ct]] = 0u;
-            named_bar_sync(15, CT);
-        }
-    } else if (MP == 8 && p.C > 1) {
-        // Split-K fix-up by owners, MMA variant with more than LAST_MAX units
-        // per CTA (128 outputs per row group: the sums are the heavy part, so
-        // they are shared out evenly).  (1) Publish: after a
-        // CTA barrier (which orders every thread's partial stores before it),
-        // fire-and-forget release reductions on the counters, one per unit of
-        // this CTA (measured: the small FP8 layers ~2 % faster than a fence
-        // followed by plain atomics).  (2) Finish: row
-        // group g belongs to CTA g mod P, P owner CTAs (below) with an even
-        // share each.  Its counters are polled in parallel, one thread per
-        // owned row group (bounded), and then each output sums its C partials
-        // in ascending chunk order.
-        named_bar_sync(15, CT);
-        for (int i = ct; i < n_units; i += CT) red_release_add_u32(counters + int((u_lo + i) % p.G), 1u);
+    if (p.C > 1) {
+        // Split-K fix-up.  Row group g belongs to CTA g mod P, P owner CTAs
+        // (below) with an even share each.  Thread ct takes output o of owned
+        // row groups e0, e0 + ES, ... (up to four at a time): it loads their C
+        // partial slots (up to eight chunks each; many chunks -- down: 17 --
+        // one row group at a time with up to 24 slots in flight), reloads any
+        // slot still empty (bounded), sums them in ascending chunk order,
+        // writes y and empties the slots again.  No counter, fence or barrier
+        // is involved: a partial is usable as soon as its store reaches L2
+        // (measured against a release-increment per unit at the end of each
+        // CTA's range, counter polls and then the loads: the decode stack 7 %
+        // faster at M = 1 and M = 8, every layer 0.5-2 us faster per launch).
+        //
         // Owners: the first half of the grid (about one CTA per SM) when each of
         // them then owns at most one round (4 * ES) of row groups, so that the
-        // other half leaves right after publishing and the next kernel's CTAs
-        // take their slots and start streaming during this tail (measured:
-        // qkv / o_proj / down 6 % faster); otherwise every CTA owns some.
+        // other half leaves right after its main loop and the next kernel's
+        // CTAs take their slots and start streaming during this tail
+        // (measured: qkv / o_proj / down 6 % faster); otherwise every CTA owns
+        // some.
         constexpr int ES = CT / NOUT;
         const int PH = (int(gridDim.x) + 1) / 2;
         const int P = (p.G + PH - 1) / PH <= 4 * ES ? PH : int(gridDim.x);
         const int n_own =
             (p.G > int(blockIdx.x) && int(blockIdx.x) < P) ? (p.G - 1 - int(blockIdx.x)) / P + 1 : 0;
-        for (int e = ct; e < n_own; e += CT) {
-            const unsigned int *cnt = counters + int(blockIdx.x) + e * P;
-            if (ld_acquire_u32(cnt) == unsigned(p.C)) continue;
-            const uint64_t t0 = globaltimer_ns();
-            for (;;) {
-                __nanosleep(32);
-                if (ld_acquire_u32(cnt) == unsigned(p.C) || flags[0]) break;
-                if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
-                    flags[0] = 1;
-                    atomicOr(&ctrl->err, ERR_TIMEOUT);
-                    break;
-                }
-            }
-        }
-        // The polling threads' acquire loads precede this barrier, which
-        // orders them before every thread's partial loads.
-        named_bar_sync(15, CT);
-        // Thread ct sums output o of owned row groups e0, e0 + ES, ... (up to
-        // four at a time), loading eight chunks of each before adding them so
-        // that up to 32 loads are in flight per thread.
         constexpr int CB = 8;
         const int o = ct % NOUT;
         if (p.C > CB) {
-            // Many chunks (down: 17): one row group at a time with up to 24 of
-            // its partials in flight -- one round trip to L2 instead of three
-            // (measured: down 13.99 -> 13.38 us per launch at M = 8).
             constexpr int CL = 24;
             for (int e = ct / NOUT; e < n_own; e += ES) {
                 const int gq = int(blockIdx.x) + e * P;
                 float acc = 0.f;
                 for (int c0 = 0; c0 < p.C; c0 += CL) {
+                    float *slot = partials + ((size_t)gq * p.C + c0) * NOUT + o;
                     float v[CL];
+                    bool miss = false;
+#pragma unroll
+                    for (int k = 0; k < CL; ++k) v[k] = c0 + k < p.C ? ld_relaxed_f32(slot + k * NOUT) : 0.f;
+#pragma unroll
+                    for (int k = 0; k < CL; ++k) miss |= __float_as_uint(v[k]) == PARTIAL_EMPTY;
+                    if (miss) {
+                        const uint64_t t0 = globaltimer_ns();
+                        while (miss) {
+                            __nanosleep(32);
+                            miss = false;
+#pragma unroll
+                            for (int k = 0; k < CL; ++k)
+                                if (__float_as_uint(v[k]) == PARTIAL_EMPTY) v[k] = ld_relaxed_f32(slot + k * NOUT);
+#pragma unroll
+                            for (int k = 0; k < CL; ++k) miss |= __float_as_uint(v[k]) == PARTIAL_EMPTY;
+                            if (miss && globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+                                flags[0] = 1;
+                                atomicOr(&ctrl->err, ERR_TIMEOUT);
+                                break;
+                            }
+                        }
+                    }
 #pragma unroll
                     for (int k = 0; k < CL; ++k)
-                        v[k] = c0 + k < p.C ? ld_cg_f32(partials + ((size_t)gq * p.C + c0 + k) * NOUT + o) : 0.f;
-#pragma unroll
-                    for (int k = 0; k < CL; ++k)
-                        if (c0 + k < p.C) acc += v[k];
+                        if (c0 + k < p.C) {
+                            acc += v[k];
+                            st_relaxed_f32(slot + k * NOUT, __uint_as_float(PARTIAL_EMPTY));
+                        }
                 }
                 finalize<FMT, MP, F16OUT, ARGMAX>(p, gq, o, acc, best);
             }
@@ -748,25 +668,54 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
             }
             for (int c0 = 0; c0 < p.C; c0 += CB) {
                 float v[4][CB];
+                bool miss = false;
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
 #pragma unroll
                     for (int k = 0; k < CB; ++k)
                         v[j][k] = (gg[j] >= 0 && c0 + k < p.C)
-                                      ? ld_cg_f32(partials + ((size_t)gg[j] * p.C + c0 + k) * NOUT + o)
+                                      ? ld_relaxed_f32(partials + ((size_t)gg[j] * p.C + c0 + k) * NOUT + o)
                                       : 0.f;
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
 #pragma unroll
+                    for (int k = 0; k < CB; ++k) miss |= __float_as_uint(v[j][k]) == PARTIAL_EMPTY;
+                if (miss) {
+                    const uint64_t t0 = globaltimer_ns();
+                    while (miss) {
+                        __nanosleep(32);
+                        miss = false;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+#pragma unroll
+                            for (int k = 0; k < CB; ++k)
+                                if (__float_as_uint(v[j][k]) == PARTIAL_EMPTY)
+                                    v[j][k] = ld_relaxed_f32(partials + ((size_t)gg[j] * p.C + c0 + k) * NOUT + o);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+#pragma unroll
+                            for (int k = 0; k < CB; ++k) miss |= __float_as_uint(v[j][k]) == PARTIAL_EMPTY;
+                        if (miss && globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+                            flags[0] = 1;
+                            atomicOr(&ctrl->err, ERR_TIMEOUT);
+                            break;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
                     for (int k = 0; k < CB; ++k)
-                        if (c0 + k < p.C) acc[j] += v[j][k];
+                        if (gg[j] >= 0 && c0 + k < p.C) {
+                            acc[j] += v[j][k];
+                            st_relaxed_f32(partials + ((size_t)gg[j] * p.C + c0 + k) * NOUT + o,
+                                           __uint_as_float(PARTIAL_EMPTY));
+                        }
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 if (gg[j] >= 0) finalize<FMT, MP, F16OUT, ARGMAX>(p, gg[j], o, acc[j], best);
         }
-        named_bar_sync(15, CT);
-        for (int e = ct; e < n_own; e += CT) counters[int(blockIdx.x) + e * P] = 0u;
     }
 
     if constexpr (ARGMAX) {

@@ -6,7 +6,7 @@
 // unsafe (inside a memory-pool or arena allocator that owns all device memory,
 // in a process whose allocator is frozen after start-up, or under a strict
 // no-allocation policy on the serving path).  This entry point serves them: its
-// scratch memory (split-K partial sums, row-group counters, the control block)
+// scratch memory (the control block and the split-K partial slots)
 // is a file-scope static __device__ array of fixed size, created when the
 // library is loaded and kept by every GPU that loads it until the process
 // exits.  The caller passes only inputs and outputs.
@@ -16,7 +16,8 @@
 // encoder and the SM count; make that first call before any stream capture.
 // Every call shares the one array and leaves its contents behind, so calls
 // whose kernels overlap on the GPU (different streams, or different host
-// threads) race on it; each call clears the part that must start at zero.
+// threads) race on it; each call resets the part it uses (the control block
+// to zero, the partial slots it needs to empty) before its kernel.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -30,8 +31,8 @@
 
 namespace {
 
-// 8 MiB: the control block and row-group counters of the workspace layout
-// (about 1 MiB) plus about 7 MiB of split-K partial sums.
+// 8 MiB: the 4 KiB control block of the workspace layout and 8,384,512 bytes
+// of split-K partial slots.
 constexpr size_t NOALLOC_SCRATCH_BYTES = size_t(8) << 20;
 static_assert(NOALLOC_SCRATCH_BYTES > sk::WS_PARTIAL_OFFSET, "scratch must hold the fixed workspace header");
 
@@ -99,7 +100,6 @@ sk_status nvfp4_gemm_noalloc(const void *x, const uint8_t *W_codes, const uint8_
     if (M < 1 || M > 8 || N < 0 || K < 0) return SK_ERR_INVALID_ARG;
     if (!x || !W_codes || !W_scales || !y) return SK_ERR_INVALID_ARG;
     if (K % 256) return SK_ERR_UNSUPPORTED_SHAPE;
-    if (size_t(N) > sk::WS_MAX_ROWGROUPS * sk::RG) return SK_ERR_UNSUPPORTED_SHAPE;
     if (!na_aligned(x, 16) || !na_aligned(W_codes, 16) || !na_aligned(W_scales, 16)) return SK_ERR_MISALIGNED;
     if (!na_aligned(y, 4)) return SK_ERR_MISALIGNED;
     NoAllocDevice *d = nullptr;
@@ -115,11 +115,12 @@ sk_status nvfp4_gemm_noalloc(const void *x, const uint8_t *W_codes, const uint8_
     if (N == 0) return SK_OK;
     if (K == 0) return cudaMemsetAsync(y, 0, size_t(M) * N * 4, s) == cudaSuccess ? SK_OK : SK_ERR_CUDA;
 
-    // The control block and the row-group counters must start at zero.  A
-    // completed call leaves them at zero, but the array is shared by every
-    // call, so clear them here too (an aborted call may have left counts).
+    // The control block must start at zero and the partial slots the kernel
+    // uses empty.  A completed call leaves them so, but the array is shared by
+    // every call, so reset them here too (an aborted call may have left
+    // partial sums behind).
     if (cudaMemsetAsync(d->scratch, 0, sk::WS_CTRL_BYTES, s) != cudaSuccess ||
-        cudaMemsetAsync(d->scratch + sk::WS_CTRL_BYTES, 0, size_t(G) * 4, s) != cudaSuccess)
+        (C > 1 && sk::empty_partials(d->scratch, size_t(G * C) * sk::unit_partial_bytes(mp), s) != cudaSuccess))
         return SK_ERR_CUDA;
 
     sk::Params p = {};

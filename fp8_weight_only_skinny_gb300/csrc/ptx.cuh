@@ -176,41 +176,20 @@ __device__ __forceinline__ uint4 ld_global_v4(const void *p) {
     return v;
 }
 
-// Acquire load at GPU scope (pairs with the fence + atomic of the writer).
-__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int *p) {
-    unsigned int v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+// Relaxed load / store at GPU scope: coherent at L2 for a value another CTA of
+// the grid stores or polls (each split-K partial slot is self-describing, so
+// no ordering between slots is needed).
+__device__ __forceinline__ float ld_relaxed_f32(const float *p) {
+    float v;
+    asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
     return v;
 }
 
-// Release reduction at GPU scope: after a CTA barrier, it orders every store
-// the CTA made before the barrier ahead of the increment (the release is
-// cumulative over what the barrier made visible to this thread).
-__device__ __forceinline__ void red_release_add_u32(unsigned int *p, unsigned int v) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Fetch-and-add at GPU scope with acquire-release semantics: releases the
-// stores ordered before it (a preceding CTA barrier makes them cumulative) and
-// acquires those released by earlier increments of the same counter.
-__device__ __forceinline__ unsigned int atom_add_acq_rel_u32(unsigned int *p, unsigned int v) {
-    unsigned int old;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
-}
-
-// Bring the line holding `p` into L1 (no register, no wait).
-__device__ __forceinline__ void prefetch_l1(const void *p) {
-    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+__device__ __forceinline__ void st_relaxed_f32(float *p, float v) {
+    asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
 // Coherent-at-L2 load for data written by other CTAs of the same grid.
-__device__ __forceinline__ float ld_cg_f32(const float *p) {
-    float v;
-    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
-    return v;
-}
-
 __device__ __forceinline__ unsigned long long ld_cg_u64(const unsigned long long *p) {
     unsigned long long v;
     asm volatile("ld.global.cg.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");

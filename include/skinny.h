@@ -46,7 +46,8 @@
  *   - One stream at a time per workspace: calls whose kernels overlap in time
  *     on different streams of the same device race on the workspace.  Each
  *     kernel also expects its whole grid (two CTAs per SM) to be resident at
- *     once -- its split-K owners wait on the other CTAs of the grid -- so
+ *     once -- its split-K owners wait for partial sums from the other CTAs of
+ *     the grid -- so
  *     another kernel that occupies SMs at the same time can make those waits
  *     run out (SK_ERR_TIMEOUT) instead of finishing.  Streams that must run
  *     at the same time each get a workspace of their own with
@@ -90,7 +91,7 @@ extern "C" {
 typedef enum {
     SK_OK = 0,
     SK_ERR_INVALID_ARG = 1,       /* NULL pointer, M outside 1..8, negative N/K */
-    SK_ERR_UNSUPPORTED_SHAPE = 2, /* K not a multiple of 256 (NVFP4) / 128 (FP8), or N too large */
+    SK_ERR_UNSUPPORTED_SHAPE = 2, /* K not a multiple of 256 (NVFP4) / 128 (FP8) */
     SK_ERR_MISALIGNED = 3,        /* a pointer breaks the alignment rule of its argument */
     SK_ERR_NOT_INITIALIZED = 4,   /* no sk_init() on the current device */
     SK_ERR_CUDA = 5,              /* a CUDA runtime call or launch failed */
@@ -99,7 +100,9 @@ typedef enum {
 } sk_status;
 
 /*
- * Allocate (cudaMalloc) and zero the workspace of the CURRENT device.
+ * Allocate (cudaMalloc) and initialise the workspace of the CURRENT device
+ * (a zeroed 4 KiB control block followed by split-K partial-sum slots, all
+ * marked empty; every call leaves them empty again).
  * workspace_bytes = 0 picks the default, 64 MiB, which covers the largest call
  * below (N = 151936, K = 5120, M = 8 needs about 25 MB).  Calling it again on
  * the same device frees and re-creates the workspace (wait for all work of the
@@ -110,7 +113,7 @@ SK_API sk_status sk_init(size_t workspace_bytes);
 
 /*
  * A workspace of its own for `stream` (a cudaStream_t; NULL = the legacy
- * default stream) on the CURRENT device, allocated (cudaMalloc) and zeroed
+ * default stream) on the CURRENT device, allocated (cudaMalloc) and initialised
  * like sk_init's; workspace_bytes = 0 removes the stream's workspace (its calls
  * fall back to the device's).  Calling it again replaces the workspace (after
  * synchronising the stream).  Every later call on that stream -- linear
@@ -316,22 +319,22 @@ SK_API void sk_inject_wait_timeout(int enable);
  *   Arguments, layouts and results are those of nvfp4_gemm (FP32 output).
  *   SK_ERR_WORKSPACE: the split-K partial sums of this shape do not fit the
  *   array.  With K > 1024 a call needs
- *       ceil(N/16) * ceil(K/1024) * 64 * m  bytes  <=  7,335,936 bytes,
+ *       ceil(N/16) * ceil(K/1024) * 64 * m  bytes  <=  8,384,512 bytes,
  *   where m is the token slots of the kernel variant that runs: m = 8 for
  *   every M >= 2, and for M = 1 unless the single-token variant is chosen
  *   (sk_set_variant(SK_VARIANT_SIMT), or SK_VARIANT_AUTO on a shape with at
  *   least 96 units of 16 rows x 1024 k per CTA), where m = 1.  For example
- *   at M = 2 and K = 5120, N <= 45,840 fits and N = 45,856 is rejected.
+ *   at M = 2 and K = 5120, N <= 52,400 fits and N = 52,416 is rejected.
  *   K <= 1024 needs no partial sums.
  *   The first call on a device (with that device current) looks up the
  *   array's device address (cudaGetSymbolAddress), the tensor-map encoder and
  *   the SM count: make it before any stream capture.  All calls share the one
- *   array and leave their partial sums in it; each call clears the counters it
- *   needs before its kernel runs.  Calls whose kernels overlap on the GPU
- *   (different streams or host threads) race on the array.  Bounded-wait
- *   timeouts of this entry point are not reported by sk_last_device_error();
- *   the next call starts from a cleared control block and counters, so it is
- *   correct again.
+ *   array; each call resets the control block and marks the partial-sum slots
+ *   it needs empty before its kernel runs (one small fill kernel).  Calls
+ *   whose kernels overlap on the GPU (different streams or host threads) race
+ *   on the array.  Bounded-wait timeouts of this entry point are not reported
+ *   by sk_last_device_error(); the next call starts from a reset control block
+ *   and empty slots, so it is correct again.
  */
 SK_API sk_status nvfp4_gemm_noalloc(const void *x, const uint8_t *W_codes, const uint8_t *W_scales,
                                     float W_gscale, float *y, int M, int N, int K, void *stream);

@@ -84,10 +84,6 @@ def test_fp8_k_must_be_multiple_of_128(K):
     assert _f8(K=K) == UNSUPPORTED
 
 
-def test_n_beyond_the_counter_capacity():
-    assert _nv(N=(1 << 22) + 1) == UNSUPPORTED
-
-
 def test_misaligned_pointers_rejected():
     assert _nv(x=A + 8) == MISALIGNED
     assert _nv(c=A + 4) == MISALIGNED

@@ -1,7 +1,7 @@
-"""GPU parity at the largest N the library accepts: 2^22 rows = 2^18 row
-groups of 16, the capacity of the split-K row-group counters, with two
-k-chunks so that every counter is used; and the same shape reported, not
-run, where its partial sums exceed the workspace."""
+"""GPU parity at a very large N: 2^22 rows = 2^18 row groups of 16, with two
+k-chunks so that every row group goes through the split-K fix-up (2^19 units
+of partial sums at M = 1); and the same shape reported, not run, where its
+partial sums exceed the workspace."""
 import numpy as np
 import pytest
 
@@ -31,7 +31,7 @@ def _edge_rows(n_random, seed):
     return np.unique(np.concatenate([fixed, np.random.default_rng(seed).choice(N_MAX, n_random, replace=False)]))
 
 
-def test_nvfp4_at_the_row_group_capacity(sk):
+def test_nvfp4_at_four_million_rows(sk):
     import torch
 
     g = torch.Generator(device="cuda:0")
@@ -53,7 +53,7 @@ def test_nvfp4_at_the_row_group_capacity(sk):
     torch.cuda.empty_cache()
 
 
-def test_fp8_at_the_row_group_capacity(sk):
+def test_fp8_at_four_million_rows(sk):
     import torch
 
     g = torch.Generator(device="cuda:0")

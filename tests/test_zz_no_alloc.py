@@ -67,12 +67,12 @@ def test_noalloc_matches_nvfp4_gemm_on_two_calls(sk, M, K, N):
 @pytest.mark.parametrize("M", [2, 8])
 def test_noalloc_scratch_limit_boundary(sk, M):
     """At K = 5120 (five 1024-k chunks) every M >= 2 uses 8 token slots, so the
-    partial sums take ceil(N/16) * 5 * 512 bytes of the 7,335,936 available:
-    N = 45,840 fits and N = 45,856 (one more row group) is rejected with
+    partial sums take ceil(N/16) * 5 * 512 bytes of the 8,384,512 available:
+    N = 52,400 fits and N = 52,416 (one more row group) is rejected with
     SK_ERR_WORKSPACE before anything is launched."""
     import torch
 
-    K, N_in, N_out = 5120, 45840, 45856
+    K, N_in, N_out = 5120, 52400, 52416
     x = torch.zeros((M, K), dtype=torch.float16, device="cuda:0")
     codes = torch.zeros((N_out, K // 2), dtype=torch.uint8, device="cuda:0")
     scales = torch.full((N_out, K // 16), 0x38, dtype=torch.uint8, device="cuda:0")
