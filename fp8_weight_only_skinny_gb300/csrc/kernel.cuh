@@ -542,6 +542,24 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
     float *gred = red + q * RED;
     unsigned long long best = 0;                       // ARGMAX: best key of token ct % MP
 
+    // Activations of this CTA's first and last k-chunk into L2 while the
+    // previous kernel finishes (one 128-byte line per thread).  L2 is the
+    // point of coherence, so a line the previous kernel writes afterwards is
+    // still read correctly after the wait below; x that is already in L2 (the
+    // usual case when the previous kernel produced it) makes this a no-op.
+    // Measured on the decode stack, where every layer's x is cold: 2.5 %
+    // faster at M = 8.
+    {
+        constexpr int LINES = KC * 2 / 128;
+        if (ct < p.M * LINES && n_units > 0) {
+            const int m = ct / LINES, l = ct % LINES;
+            const int k = c_lo * KC + l * 64;
+            if (k < p.K) prefetch_l2(p.x + size_t(m) * p.K + k);
+            const int c_last = int((u_hi - 1) / p.G);
+            const int k2 = c_last * KC + l * 64;
+            if (c_last != c_lo && k2 < p.K) prefetch_l2(p.x + size_t(m) * p.K + k2);
+        }
+    }
     pdl_wait_primary();   // x, y and the workspace belong to the previous kernel until here
 
     XRegs<FMT, MP> xr;

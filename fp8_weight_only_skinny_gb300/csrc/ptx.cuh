@@ -189,6 +189,11 @@ __device__ __forceinline__ void st_relaxed_f32(float *p, float v) {
     asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
+// Bring the line holding `p` into L2 (a hint: no register, no wait, no fault).
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // Coherent-at-L2 load for data written by other CTAs of the same grid.
 __device__ __forceinline__ unsigned long long ld_cg_u64(const unsigned long long *p) {
     unsigned long long v;
