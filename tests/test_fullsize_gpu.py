@@ -59,7 +59,7 @@ def _cols(N, n=192, seed=0):
 
 
 @pytest.mark.parametrize("name,K,N", SHAPES)
-@pytest.mark.parametrize("M", [1, 8])
+@pytest.mark.parametrize("M", [1, 2, 4, 8])
 def test_nvfp4_full_size(sk, name, K, N, M):
     """Every one of the N output columns against the oracle (FP32 output)."""
     import torch
@@ -73,7 +73,7 @@ def test_nvfp4_full_size(sk, name, K, N, M):
 
 
 @pytest.mark.parametrize("name,K,N", SHAPES)
-@pytest.mark.parametrize("M", [1, 8])
+@pytest.mark.parametrize("M", [1, 2, 4, 8])
 def test_fp8_full_size(sk, name, K, N, M):
     """Every one of the N output columns against the oracle (FP16 output, as
     the benchmark's stack writes it)."""
