@@ -64,28 +64,6 @@ sk_status resolve_encode() {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// 2-D map over a row-major byte matrix viewed as u32 words:
-// dims {row_bytes/4, rows}, row stride row_bytes, box {box_words, 16}.
-bool encode_map(CUtensorMap *m, const void *ptr, uint64_t row_bytes, uint64_t rows, uint32_t box_words) {
-    cuuint64_t dims[2] = {row_bytes / 4, rows};
-    cuuint64_t strides[1] = {row_bytes};
-    cuuint32_t box[2] = {box_words, uint32_t(sk::RG)};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(ptr), dims, strides, box,
-                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
-// Current device's state, or null if sk_init() has not run on it.
-DeviceState *current(int *dev_out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return nullptr;
-    if (dev_out) *dev_out = dev;
-    DeviceState *d = &g_dev[dev];
-    return d->ws ? d : nullptr;
-}
-
 // The workspace a call on `s` uses on the current device: the stream's own if
 // it has one (then `own` is set), else the device's; false if neither exists.
 struct WsRef {
@@ -195,13 +173,12 @@ sk_status run(Kind kind, const void *x, const uint8_t *codes, const void *scales
 
     CUtensorMap tm_codes, tm_scales;
     if (nv) {
-        if (!encode_map(&tm_codes, codes, uint64_t(K) / 2, uint64_t(N), sk::Traits<sk::NVFP4>::CODE_BOX_X) ||
-            !encode_map(&tm_scales, scales, uint64_t(K) / 16, uint64_t(N), sk::Traits<sk::NVFP4>::SCALE_BOX_X))
+        if (!sk::encode_weight_maps(g_encode, true, codes, scales, K, N, &tm_codes, &tm_scales))
             return SK_ERR_CUDA;
         if (sk::launch_nvfp4(mp, f16, am, tm_codes, tm_scales, p, grid, s, pdl, coop) != cudaSuccess)
             return SK_ERR_CUDA;
     } else {
-        if (!encode_map(&tm_codes, codes, uint64_t(K), uint64_t(N), sk::Traits<sk::FP8>::CODE_BOX_X))
+        if (!sk::encode_weight_maps(g_encode, false, codes, nullptr, K, N, &tm_codes, nullptr))
             return SK_ERR_CUDA;
         if (sk::launch_fp8(mp, f16, tm_codes, p, grid, s, pdl, coop) != cudaSuccess) return SK_ERR_CUDA;
     }
@@ -232,6 +209,38 @@ cudaError_t empty_partials(unsigned char *ws, size_t bytes, cudaStream_t stream)
 // gate_up 5120x34816 at 36 units per CTA, NVFP4 lm_head at 156), because its
 // per-unit arithmetic is lighter while its fix-up and start-up are not.
 int take_inject_stall() { return g_inject_stall.exchange(0); }
+
+bool encode_weight_maps(PFN_cuTensorMapEncodeTiled_v12000 enc, bool nvfp4, const void *codes,
+                        const void *scales, int K, int N, CUtensorMap *tm_codes, CUtensorMap *tm_scales) {
+    // Every map views its bytes as u32 words, reads out of bounds as zero and
+    // has boxes of one unit's tile (the tile layouts beside Traits, kernel.cuh).
+    auto enc3 = [&](CUtensorMap *m, const void *ptr, const cuuint64_t (&dims)[3], const cuuint64_t (&strides)[2],
+                    const cuuint32_t (&box)[3]) {
+        const cuuint32_t estr[3] = {1, 1, 1};
+        return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    const uint64_t rows = uint64_t(N), row_bytes = nvfp4 ? uint64_t(K) / 2 : uint64_t(K);
+    if (!nvfp4) {
+        // codes {word in a 128-byte segment, row, segment}: box [8 segments][16 rows][128 B]
+        return enc3(tm_codes, codes, {32, rows, row_bytes / 128}, {row_bytes, 128},
+                    {32, uint32_t(RG), uint32_t(Traits<FP8>::SEGS)});
+    }
+    // codes {word in a 128-byte segment, segment, row}: box [16 rows][4 segments][128 B]
+    if (!enc3(tm_codes, codes, {32, row_bytes / 128, rows}, {128, row_bytes},
+              {32, uint32_t(Traits<NVFP4>::SEGS), uint32_t(RG)}))
+        return false;
+    // scales {word, row}: box [16 rows][64 B], 64-byte swizzle
+    const uint64_t srow = uint64_t(K) / 16;
+    const cuuint64_t dims[2] = {srow / 4, rows};
+    const cuuint64_t strides[1] = {srow};
+    const cuuint32_t box[2] = {uint32_t(Traits<NVFP4>::SCALE_BOX_X), uint32_t(RG)};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(tm_scales, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(scales), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 bool encode_2d_u16(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint32_t box_cols,
                    uint32_t box_rows) {

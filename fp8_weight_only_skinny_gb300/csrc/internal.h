@@ -1,6 +1,7 @@
 // internal.h -- declarations shared by the host translation units of libskinny.
 #pragma once
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -16,6 +17,13 @@ cudaError_t launch_nvfp4(int mp, bool f16out, bool argmax, const CUtensorMap &tm
                          cudaStream_t stream, bool pdl, bool coop);
 cudaError_t launch_fp8(int mp, bool f16out, const CUtensorMap &tm_codes, const Params &p, int grid,
                        cudaStream_t stream, bool pdl, bool coop);
+
+// The TMA maps of a linear call's weights (K, N as in the call; K a multiple
+// of 256 for NVFP4, of 128 for FP8): NVFP4 codes and scales, or FP8 codes
+// (tm_scales unused), with the tile layouts and swizzles the kernel reads.
+// `enc` is the driver's cuTensorMapEncodeTiled; false if it rejects a map.
+bool encode_weight_maps(PFN_cuTensorMapEncodeTiled_v12000 enc, bool nvfp4, const void *codes,
+                        const void *scales, int K, int N, CUtensorMap *tm_codes, CUtensorMap *tm_scales);
 
 // 2-D TMA map over a row-major matrix of 16-bit elements [rows][cols]
 // (row stride cols * 2 bytes), box {box_cols, box_rows}, out-of-bounds reads

@@ -80,16 +80,6 @@ sk_status setup_current(NoAllocDevice **out) {
 
 bool na_aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-bool na_encode_map(CUtensorMap *m, const void *ptr, uint64_t row_bytes, uint64_t rows, uint32_t box_words) {
-    cuuint64_t dims[2] = {row_bytes / 4, rows};
-    cuuint64_t strides[1] = {row_bytes};
-    cuuint32_t box[2] = {box_words, uint32_t(sk::RG)};
-    cuuint32_t estr[2] = {1, 1};
-    return g_na_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 extern "C" {
@@ -139,8 +129,7 @@ sk_status nvfp4_gemm_noalloc(const void *x, const uint8_t *W_codes, const uint8_
     p.U = G * C;
     p.stall = sk::take_inject_stall();   // the test hook of sk_inject_wait_timeout()
     CUtensorMap tm_codes, tm_scales;
-    if (!na_encode_map(&tm_codes, W_codes, uint64_t(K) / 2, uint64_t(N), sk::Traits<sk::NVFP4>::CODE_BOX_X) ||
-        !na_encode_map(&tm_scales, W_scales, uint64_t(K) / 16, uint64_t(N), sk::Traits<sk::NVFP4>::SCALE_BOX_X))
+    if (!sk::encode_weight_maps(g_na_encode, true, W_codes, W_scales, K, N, &tm_codes, &tm_scales))
         return SK_ERR_CUDA;
     sk::take_weights_written(s);   // launched without PDL anyway; clears a quantizer's mark
     if (sk::launch_nvfp4(mp, false, false, tm_codes, tm_scales, p, grid, s, false, false) != cudaSuccess)

@@ -64,11 +64,22 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
-// Bring one tile of a tensor map into L2 (no destination, no completion), with
-// an L2 eviction policy.
-__device__ __forceinline__ void tma_prefetch_l2_2d(const void *tmap, int32_t c0, int32_t c1, uint64_t policy) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile.L2::cache_hint [%0, {%1, %2}], %3;"
-                 ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "l"(policy) : "memory");
+// 3-D tiled bulk tensor load into this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint32_t bar,
+                                            int32_t c0, int32_t c1, int32_t c2, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// Bring one tile of a 3-D tensor map into L2 (no destination, no completion),
+// with an L2 eviction policy.
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void *tmap, int32_t c0, int32_t c1, int32_t c2,
+                                                   uint64_t policy) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile.L2::cache_hint [%0, {%1, %2, %3}], %4;"
+                 ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "l"(policy) : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
