@@ -167,6 +167,7 @@ sk_status run(Kind kind, const void *x, const uint8_t *codes, const void *scales
     // summation order, so it follows from the shape alone: a token's outputs
     // must not depend on the other tokens of the call.
     p.fp8_kpairs = (!nv && p.U >= 7LL * grid) ? 1 : 0;
+    const bool xwide = sk::use_wide_x(x, M);
     if (p.C > 1) {
         const size_t need = size_t(p.U) * sk::unit_partial_bytes(mp);
         if (sk::WS_PARTIAL_OFFSET + need > wr.bytes) return SK_ERR_WORKSPACE;
@@ -185,12 +186,12 @@ sk_status run(Kind kind, const void *x, const uint8_t *codes, const void *scales
     if (nv) {
         if (!sk::encode_weight_maps(g_encode, true, codes, scales, K, N, &tm_codes, &tm_scales))
             return SK_ERR_CUDA;
-        if (sk::launch_nvfp4(mp, f16, am, tm_codes, tm_scales, p, grid, s, pdl, coop) != cudaSuccess)
+        if (sk::launch_nvfp4(mp, xwide, f16, am, tm_codes, tm_scales, p, grid, s, pdl, coop) != cudaSuccess)
             return SK_ERR_CUDA;
     } else {
         if (!sk::encode_weight_maps(g_encode, false, codes, nullptr, K, N, &tm_codes, nullptr))
             return SK_ERR_CUDA;
-        if (sk::launch_fp8(mp, f16, tm_codes, p, grid, s, pdl, coop) != cudaSuccess) return SK_ERR_CUDA;
+        if (sk::launch_fp8(mp, xwide, f16, tm_codes, p, grid, s, pdl, coop) != cudaSuccess) return SK_ERR_CUDA;
     }
     return SK_OK;
 }
@@ -300,6 +301,10 @@ bool take_weights_written(cudaStream_t stream) {
 unsigned char *workspace_for(cudaStream_t stream) {
     WsRef r;
     return workspace_ref(stream, &r) ? r.ws : nullptr;
+}
+
+bool use_wide_x(const void *x, int M) {
+    return M >= 4 && reinterpret_cast<uintptr_t>(x) % 32 == 0;
 }
 
 int choose_mp(int M, bool nvfp4, long long U, long long P) {

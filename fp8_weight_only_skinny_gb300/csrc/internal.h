@@ -12,10 +12,11 @@ struct Params;
 // Launch one kernel of the given format.  mp: token slots of the variant
 // (1 = single-token SIMT variant; 8 = tensor-core variant); pdl: programmatic
 // dependent launch; coop: cooperative launch (the whole grid co-resident).
-cudaError_t launch_nvfp4(int mp, bool f16out, bool argmax, const CUtensorMap &tm_codes,
+// xwide: 32-byte activation loads in the tensor-core variant (use_wide_x).
+cudaError_t launch_nvfp4(int mp, bool xwide, bool f16out, bool argmax, const CUtensorMap &tm_codes,
                          const CUtensorMap &tm_scales, const Params &p, int grid,
                          cudaStream_t stream, bool pdl, bool coop);
-cudaError_t launch_fp8(int mp, bool f16out, const CUtensorMap &tm_codes, const Params &p, int grid,
+cudaError_t launch_fp8(int mp, bool xwide, bool f16out, const CUtensorMap &tm_codes, const Params &p, int grid,
                        cudaStream_t stream, bool pdl, bool coop);
 
 // The TMA maps of a linear call's weights (K, N as in the call; K a multiple
@@ -57,6 +58,15 @@ bool take_weights_written(cudaStream_t stream);
 // The workspace a call on `stream` uses on the current device: the stream's
 // own (sk_stream_workspace), else the device's (sk_init); null if neither.
 unsigned char *workspace_for(cudaStream_t stream);
+
+// Whether the tensor-core variant loads the activations 32 bytes per lane
+// and instruction (kernel.cuh, load_x) instead of 16: for M >= 4 and x
+// 32-byte aligned.  Half the load instructions and line look-ups before the
+// first MMA of each k-chunk; measured on the decode layers (cold L2): 0.25-0.5
+// us faster per launch at M = 8 on the small shapes (decode stack 1.4 %), a
+// little faster at M = 4, neutral at M = 2, and the same code as before at M
+// = 1.  The values loaded, and so the results, do not change.
+bool use_wide_x(const void *x, int M);
 
 // Token slots of the kernel variant for an M-token call of U units on a grid
 // of P CTAs: 1 (SIMT) or 8 (tensor-core), by the process-wide variant setting.

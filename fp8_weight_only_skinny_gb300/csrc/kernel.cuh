@@ -243,7 +243,7 @@ struct XRegs {
     uint32_t w[TOK][PIECES][WORDS];
 };
 
-template <int FMT, int MP>
+template <int FMT, int MP, bool XWIDE>
 __device__ __forceinline__ void load_x(XRegs<FMT, MP> &xr, const Params &p, int c, int warp_in_group,
                                        int lane) {
     const int kbase = c * KC;
@@ -254,15 +254,26 @@ __device__ __forceinline__ void load_x(XRegs<FMT, MP> &xr, const Params &p, int 
             const int k0 = (FMT == NVFP4) ? kbase + 256 * warp_in_group + 128 * t + 32 * q
                            : p.fp8_kpairs ? kbase + 256 * warp_in_group + 128 * (t >> 1) + 32 * q + 16 * (t & 1)
                                           : kbase + 256 * warp_in_group + 64 * t + 16 * q;
+            if constexpr (XWIDE) {   // x 32-byte aligned; k0 a multiple of 16
 #pragma unroll
-            for (int v = 0; v < XRegs<FMT, MP>::WORDS / 4; ++v) {
-                const int k = k0 + 8 * v;
-                uint4 val = make_uint4(0, 0, 0, 0);
-                if (j < p.M && k < p.K) val = ld_global_v4(p.x + size_t(j) * p.K + k);
-                xr.w[0][t][4 * v + 0] = val.x;
-                xr.w[0][t][4 * v + 1] = val.y;
-                xr.w[0][t][4 * v + 2] = val.z;
-                xr.w[0][t][4 * v + 3] = val.w;
+                for (int v = 0; v < XRegs<FMT, MP>::WORDS / 8; ++v) {
+                    const int k = k0 + 16 * v;
+                    uint32_t val[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                    if (j < p.M && k < p.K) ld_global_v8(p.x + size_t(j) * p.K + k, val);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) xr.w[0][t][8 * v + e] = val[e];
+                }
+            } else {
+#pragma unroll
+                for (int v = 0; v < XRegs<FMT, MP>::WORDS / 4; ++v) {
+                    const int k = k0 + 8 * v;
+                    uint4 val = make_uint4(0, 0, 0, 0);
+                    if (j < p.M && k < p.K) val = ld_global_v4(p.x + size_t(j) * p.K + k);
+                    xr.w[0][t][4 * v + 0] = val.x;
+                    xr.w[0][t][4 * v + 1] = val.y;
+                    xr.w[0][t][4 * v + 2] = val.z;
+                    xr.w[0][t][4 * v + 3] = val.w;
+                }
             }
         }
     } else {
@@ -477,8 +488,9 @@ __device__ __forceinline__ void finalize(const Params &p, int g, int o, float v,
 // (one k-chunk) or stores the unit's split-K partial into its slot.  The sums
 // of the C partials of each owned row group, in ascending chunk order, run
 // once per CTA after its whole range, by all consumer threads in parallel: no
-// global round trip sits on the per-unit path.
-template <int FMT, int MP, bool F16OUT, bool ARGMAX>
+// global round trip sits on the per-unit path.  XWIDE (tensor-core variant,
+// x 32-byte aligned): activations loaded 32 bytes per lane and instruction.
+template <int FMT, int MP, bool F16OUT, bool ARGMAX, bool XWIDE>
 __global__ void __launch_bounds__(CTA_THREADS, 2)
 skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
               const Params p) {
@@ -613,7 +625,7 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
     step_unit(c, g, q, p.G);                           // unit u_lo + q
     for (int i = q; i < n_units; i += NGROUPS, step_unit(c, g, NGROUPS, p.G)) {
         if (c != cur_c) {
-            load_x<FMT, MP>(xr, p, c, w, lane);
+            load_x<FMT, MP, XWIDE>(xr, p, c, w, lane);
             cur_c = c;
         }
         const int s = i % T::STAGES;

@@ -9,10 +9,10 @@ namespace sk {
 
 // pdl: programmatic dependent launch after the previous kernel on the stream;
 // coop: a cooperative launch (all CTAs co-resident before any starts).
-template <int FMT, int MP, bool F16OUT, bool ARGMAX>
+template <int FMT, int MP, bool F16OUT, bool ARGMAX, bool XWIDE>
 cudaError_t launch_variant(const CUtensorMap &tm_codes, const CUtensorMap &tm_scales, const Params &p,
                            int grid, cudaStream_t stream, bool pdl, bool coop) {
-    auto kfn = skinny_kernel<FMT, MP, F16OUT, ARGMAX>;
+    auto kfn = skinny_kernel<FMT, MP, F16OUT, ARGMAX, XWIDE>;
     constexpr size_t smem = smem_bytes<FMT, MP>();
     static bool attr_done[64] = {};
     int dev = 0;
@@ -39,10 +39,11 @@ cudaError_t launch_variant(const CUtensorMap &tm_codes, const CUtensorMap &tm_sc
 }
 
 template <int FMT, bool F16OUT, bool ARGMAX>
-cudaError_t launch_by_m(int mp, const CUtensorMap &tm_codes, const CUtensorMap &tm_scales,
+cudaError_t launch_by_m(int mp, bool xwide, const CUtensorMap &tm_codes, const CUtensorMap &tm_scales,
                         const Params &p, int grid, cudaStream_t stream, bool pdl, bool coop) {
-    if (mp == 1) return launch_variant<FMT, 1, F16OUT, ARGMAX>(tm_codes, tm_scales, p, grid, stream, pdl, coop);
-    return launch_variant<FMT, 8, F16OUT, ARGMAX>(tm_codes, tm_scales, p, grid, stream, pdl, coop);
+    if (mp == 1) return launch_variant<FMT, 1, F16OUT, ARGMAX, false>(tm_codes, tm_scales, p, grid, stream, pdl, coop);
+    if (xwide) return launch_variant<FMT, 8, F16OUT, ARGMAX, true>(tm_codes, tm_scales, p, grid, stream, pdl, coop);
+    return launch_variant<FMT, 8, F16OUT, ARGMAX, false>(tm_codes, tm_scales, p, grid, stream, pdl, coop);
 }
 
 }  // namespace sk

@@ -132,7 +132,7 @@ sk_status nvfp4_gemm_noalloc(const void *x, const uint8_t *W_codes, const uint8_
     if (!sk::encode_weight_maps(g_na_encode, true, W_codes, W_scales, K, N, &tm_codes, &tm_scales))
         return SK_ERR_CUDA;
     sk::take_weights_written(s);   // launched without PDL anyway; clears a quantizer's mark
-    if (sk::launch_nvfp4(mp, false, false, tm_codes, tm_scales, p, grid, s, false, false) != cudaSuccess)
+    if (sk::launch_nvfp4(mp, sk::use_wide_x(x, M), false, false, tm_codes, tm_scales, p, grid, s, false, false) != cudaSuccess)
         return SK_ERR_CUDA;
     return SK_OK;
 }

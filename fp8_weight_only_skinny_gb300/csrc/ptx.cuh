@@ -187,6 +187,13 @@ __device__ __forceinline__ uint4 ld_global_v4(const void *p) {
     return v;
 }
 
+// 32-byte read-only load (address 32-byte aligned).
+__device__ __forceinline__ void ld_global_v8(const void *p, uint32_t (&r)[8]) {
+    asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "l"(p));
+}
+
 // Relaxed load / store at GPU scope: coherent at L2 for a value another CTA of
 // the grid stores or polls (each split-K partial slot is self-describing, so
 // no ordering between slots is needed).

@@ -269,6 +269,43 @@ def test_rows_independent_within_a_variant(sk):
         sk.set_variant(prev)
 
 
+@pytest.mark.parametrize("M", [4, 8])
+def test_activation_alignment_does_not_change_results(sk, M):
+    """From M = 4 the tensor-core variant loads 32-byte aligned activations 32
+    bytes per lane, else 16: x at a 32-byte boundary and x 16 bytes past one
+    give bitwise the same outputs (both formats, FP32 and FP16 output, one
+    k-chunk and several), and the aligned ones match the oracle."""
+    import torch
+
+    for K, N in ((1024, 64), (5120, 200)):
+        x = synth.x_f16(M, K, seed=71 + K)
+        codes, scales, g = synth.nvfp4_weights(N, K, seed=71)
+        c8, s8 = synth.fp8_weights(N, K, seed=71)
+        cd, sd, c8d, s8d = dev(codes), dev(scales), dev(c8), dev(s8)
+        outs = []
+        for off in (0, 8):                      # halves: 0 or 16 bytes past the boundary
+            buf = torch.zeros(M * K + 16, dtype=torch.float16, device="cuda:0")
+            assert buf.data_ptr() % 32 == 0
+            xd = buf[off:off + M * K].view(M, K)
+            xd.copy_(dev(x))
+            assert (xd.data_ptr() % 32 == 0) == (off == 0)
+            got = []
+            for f16 in (False, True):
+                y = _out(M, N, f16)
+                sk.nvfp4_gemm(xd, cd, sd, float(g), y=y.t, f16_out=f16)
+                got.append(y.host("nvfp4_gemm output"))
+                y = _out(M, N, f16)
+                sk.fp8_gemm(xd, c8d, s8d, y=y.t, f16_out=f16)
+                got.append(y.host("fp8_gemm output"))
+            outs.append(got)
+        for a, b in zip(*outs):
+            assert np.array_equal(a, b)
+        y_ref, l1 = oracle.nvfp4_linear(x, codes, scales, g)
+        check(outs[0][0], y_ref, l1, False, f"nvfp4 aligned x M{M} K{K}")
+        y_ref, l1 = oracle.fp8_linear(x, c8, s8)
+        check(outs[0][1], y_ref, l1, False, f"fp8 aligned x M{M} K{K}")
+
+
 # ------------------------------------------------------ degenerate cases ---
 
 def test_k_zero_gives_zeros_and_n_zero_is_a_noop(sk):
