@@ -157,16 +157,6 @@ sk_status run(Kind kind, const void *x, const uint8_t *codes, const void *scales
     p.U = (long long)p.G * p.C;
     const int grid = grid_for(wr.num_sms, p.U);
     const int mp = sk::choose_mp(M, nv, p.U, grid);
-    // FP8 tensor-core k-piece order (unit_mma): the conflict-free order costs
-    // one more activation line per token and load, paid once per k-chunk and
-    // CTA, and saves one shared-memory wavefront per code load, paid per unit.
-    // Measured on the decode layers (cold L2): at M = 1, 2 and 4 it is 0.1-0.3
-    // us faster per launch on every shape; at M = 8 from about 7 units per CTA
-    // (qkv 5120x7168, 7.4: +0.02 us; gate_up, 36: -0.24 us), and up to 0.26 us
-    // slower below (the 4-way per-rank qkv, 1.8).  The order changes the
-    // summation order, so it follows from the shape alone: a token's outputs
-    // must not depend on the other tokens of the call.
-    p.fp8_kpairs = (!nv && p.U >= 7LL * grid) ? 1 : 0;
     const bool xwide = sk::use_wide_x(x, M);
     if (p.C > 1) {
         const size_t need = size_t(p.U) * sk::unit_partial_bytes(mp);

@@ -140,7 +140,6 @@ struct Params {
     int G, C, KB;               // row groups, k-chunks, FP8 scale row stride
     long long U;                // units = G * C
     int stall;                  // failure injection: the producer issues no copies
-    int fp8_kpairs;             // FP8 tensor-core variant: k-piece order of the lanes (unit_mma)
 };
 
 // Floats of a group's per-unit reduction buffer: MMA = 4 warps x (16 rows x 8
@@ -252,8 +251,7 @@ __device__ __forceinline__ void load_x(XRegs<FMT, MP> &xr, const Params &p, int 
 #pragma unroll
         for (int t = 0; t < XRegs<FMT, MP>::PIECES; ++t) {
             const int k0 = (FMT == NVFP4) ? kbase + 256 * warp_in_group + 128 * t + 32 * q
-                           : p.fp8_kpairs ? kbase + 256 * warp_in_group + 128 * (t >> 1) + 32 * q + 16 * (t & 1)
-                                          : kbase + 256 * warp_in_group + 64 * t + 16 * q;
+                                          : kbase + 256 * warp_in_group + 128 * (t >> 1) + 32 * q + 16 * (t & 1);
             if constexpr (XWIDE) {   // x 32-byte aligned; k0 a multiple of 16
 #pragma unroll
                 for (int v = 0; v < XRegs<FMT, MP>::WORDS / 8; ++v) {
@@ -343,21 +341,23 @@ __device__ __forceinline__ void unit_mma(float (&d)[4], const XRegs<FMT, 8> &xr,
     } else {
         const uint32_t codes = stage;
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        // Piece t of lane q: code bytes 64t + 16q of the warp's 256-byte slice
-        // of rows r and r + 8 (segment 2w + t / 2, chunk 4 (t mod 2) + q), or,
-        // with p.fp8_kpairs, bytes 128 (t / 2) + 32q + 16 (t mod 2) (same
-        // segment, chunk 2q + t mod 2).  The 16-byte loads are served a
-        // quarter-warp -- rows 2i and 2i + 1 -- at a time, and the swizzle of
-        // those two rows differs in bit 0 only: the four consecutive chunks of
-        // the first order collide two-way, the even or odd chunks of the second
-        // do not.  The second order costs the activation loads two lines per
-        // token instead of one (load_x), once per k-chunk, and the host picks
-        // it where each CTA streams enough units to repay that.
-        const uint32_t qc = p.fp8_kpairs ? 2 * q : q, tc = p.fp8_kpairs ? 1 : 4;
+        // Piece t of lane q: code bytes 128 (t / 2) + 32q + 16 (t mod 2) of the
+        // warp's 256-byte slice of rows r and r + 8 (segment 2w + t / 2, chunk
+        // 2q + t mod 2), so that each lane's two pieces of a segment are
+        // adjacent.  The 16-byte loads are served a quarter-warp -- rows 2i and
+        // 2i + 1 -- at a time, and the swizzle of those two rows differs in
+        // bit 0 only: these even or odd chunks of a segment do not collide,
+        // where four consecutive chunks per lane order (16q + 64t) would
+        // collide two-way.  The price is on the activation loads, two lines
+        // per token and instruction instead of one, once per k-chunk (load_x).
+        // Measured against the consecutive order (cold L2, both with the wide
+        // activation loads): every FP8 decode layer 0.05-0.3 us faster per
+        // launch at M = 1, 4 and 8, except the two smallest per-rank shapes
+        // at M = 8 (+0.13 us).
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
             const uint32_t off =
-                (2 * w + (t >> 1)) * 2048 + r * 128 + (((qc + uint32_t(t & 1) * tc) ^ uint32_t(r)) << 4);
+                (2 * w + (t >> 1)) * 2048 + r * 128 + ((uint32_t(2 * q + (t & 1)) ^ uint32_t(r)) << 4);
             const uint4 A = ld_shared_v4(codes + off);
             const uint4 B = ld_shared_v4(codes + off + 8 * 128);
             const uint32_t Aw[4] = {A.x, A.y, A.z, A.w};
