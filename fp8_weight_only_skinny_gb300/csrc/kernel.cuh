@@ -680,18 +680,24 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
         // CTA's range, counter polls and then the loads: the decode stack 7 %
         // faster at M = 1 and M = 8, every layer 0.5-2 us faster per launch).
         //
-        // Owners: the first half of the grid (about one CTA per SM) when each of
-        // them then owns at most one round (4 * ES) of row groups, so that the
-        // other half leaves right after its main loop and the next kernel's
-        // CTAs take their slots and start streaming during this tail
-        // (measured: qkv / o_proj / down 6 % faster); otherwise every CTA owns
-        // some.
+        // Owners: the fewest CTAs, but at least the first half of the grid
+        // (about one CTA per SM), that each sum their row groups in one round
+        // -- cap row groups: 4 * ES, or ES with more than CB chunks, which go
+        // one row group per thread at a time -- or, if even the whole grid
+        // needs more rounds, every CTA.  The other CTAs leave right after their
+        // main loop and the next kernel's CTAs take their slots and start
+        // streaming during this tail (measured: qkv / o_proj / down 6 % faster
+        // than every CTA owning).  Counting the one-row-group rounds of the
+        // many-chunk path (down: 160 owners of 2 row groups instead of 152, of
+        // which 16 held 3 and summed in two rounds) made down 0.2-0.3 us faster.
         constexpr int ES = CT / NOUT;
+        constexpr int CB = 8;
+        const int cap = p.C > CB ? ES : 4 * ES;
         const int PH = (int(gridDim.x) + 1) / 2;
-        const int P = (p.G + PH - 1) / PH <= 4 * ES ? PH : int(gridDim.x);
+        const int pmin = (p.G + cap - 1) / cap;
+        const int P = pmin <= PH ? PH : (pmin <= int(gridDim.x) ? pmin : int(gridDim.x));
         const int n_own =
             (p.G > int(blockIdx.x) && int(blockIdx.x) < P) ? (p.G - 1 - int(blockIdx.x)) / P + 1 : 0;
-        constexpr int CB = 8;
         const int o = ct % NOUT;
         if (p.C > CB) {
             constexpr int CL = 24;
