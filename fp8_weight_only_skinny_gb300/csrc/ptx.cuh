@@ -194,6 +194,15 @@ __device__ __forceinline__ void ld_global_v8(const void *p, uint32_t (&r)[8]) {
                  : "l"(p));
 }
 
+// Atomic add at GPU scope with acquire-release semantics: it releases the
+// writes ordered before it (by this thread, or by its CTA through a barrier)
+// and acquires those released by the earlier increments of the same word.
+__device__ __forceinline__ unsigned int atom_add_acq_rel_u32(unsigned int *p, unsigned int v) {
+    unsigned int old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 // Relaxed load / store at GPU scope: coherent at L2 for a value another CTA of
 // the grid stores or polls (each split-K partial slot is self-describing, so
 // no ordering between slots is needed).
