@@ -251,7 +251,7 @@ __device__ __forceinline__ void load_x(XRegs<FMT, MP> &xr, const Params &p, int 
 #pragma unroll
         for (int t = 0; t < XRegs<FMT, MP>::PIECES; ++t) {
             const int k0 = (FMT == NVFP4) ? kbase + 256 * warp_in_group + 128 * t + 32 * q
-                                          : kbase + 256 * warp_in_group + 128 * (t >> 1) + 32 * q + 16 * (t & 1);
+                                          : kbase + 256 * warp_in_group + 64 * t + 16 * q;
             if constexpr (XWIDE) {   // x 32-byte aligned; k0 a multiple of 16
 #pragma unroll
                 for (int v = 0; v < XRegs<FMT, MP>::WORDS / 8; ++v) {
@@ -292,6 +292,18 @@ __device__ __forceinline__ void load_x(XRegs<FMT, MP> &xr, const Params &p, int 
         }
     }
 }
+
+// FP8 tensor-core variant: the tile row that MMA fragment row f (0..15) holds
+// (the reduction buffer puts each D row back at its tile row).  The 16-byte
+// code loads are served a quarter-warp -- fragment rows 2i and 2i + 1 -- at a
+// time; this order gives those two rows tile rows whose swizzles (tile row
+// mod 8) differ in bit 2, so the four consecutive chunks each group of four
+// lanes reads fall in distinct banks, while the activations of one token's
+// four lanes stay in one 128-byte line.  Measured against k pieces taken in
+// pairs (also conflict-free, two activation lines per token): the per-rank
+// FP8 layers 0.2-0.3 us faster per launch at M = 8, the rest unchanged.
+// Rows f and f + 8 stay 8 apart.
+__device__ __forceinline__ int fp8_tile_row(int f) { return (f & 8) | ((f & 1) << 2) | ((f >> 1) & 3); }
 
 // ----------------------------------------------------------------------------
 // MMA path, one unit, one warp: D (16 rows x 8 tokens) of this warp's k slice.
@@ -341,23 +353,14 @@ __device__ __forceinline__ void unit_mma(float (&d)[4], const XRegs<FMT, 8> &xr,
     } else {
         const uint32_t codes = stage;
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        // Piece t of lane q: code bytes 128 (t / 2) + 32q + 16 (t mod 2) of the
-        // warp's 256-byte slice of rows r and r + 8 (segment 2w + t / 2, chunk
-        // 2q + t mod 2), so that each lane's two pieces of a segment are
-        // adjacent.  The 16-byte loads are served a quarter-warp -- rows 2i and
-        // 2i + 1 -- at a time, and the swizzle of those two rows differs in
-        // bit 0 only: these even or odd chunks of a segment do not collide,
-        // where four consecutive chunks per lane order (16q + 64t) would
-        // collide two-way.  The price is on the activation loads, two lines
-        // per token and instruction instead of one, once per k-chunk (load_x).
-        // Measured against the consecutive order (cold L2, both with the wide
-        // activation loads): every FP8 decode layer 0.05-0.3 us faster per
-        // launch at M = 1, 4 and 8, except the two smallest per-rank shapes
-        // at M = 8 (+0.13 us).
+        // Piece t of lane q: code bytes 64t + 16q of the warp's 256-byte slice
+        // (segment 2w + t / 2, chunk 4 (t mod 2) + q) of tile rows sr and
+        // sr + 8, sr = fp8_tile_row(r).
+        const uint32_t sr = uint32_t(fp8_tile_row(r));
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
             const uint32_t off =
-                (2 * w + (t >> 1)) * 2048 + r * 128 + ((uint32_t(2 * q + (t & 1)) ^ uint32_t(r)) << 4);
+                (2 * w + (t >> 1)) * 2048 + sr * 128 + ((uint32_t(4 * (t & 1) + q) ^ (sr & 7u)) << 4);
             const uint4 A = ld_shared_v4(codes + off);
             const uint4 B = ld_shared_v4(codes + off + 8 * 128);
             const uint32_t Aw[4] = {A.x, A.y, A.z, A.w};
@@ -635,7 +638,7 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
         if constexpr (MP == 8) {
             float d[4];
             unit_mma<FMT>(d, xr, stage, p, g, c, w, lane);
-            const int r = lane >> 2, qq = lane & 3;
+            const int r = (FMT == FP8) ? fp8_tile_row(lane >> 2) : lane >> 2, qq = lane & 3;
             *reinterpret_cast<float2 *>(gred + w * 128 + r * 8 + 2 * qq) = make_float2(d[0], d[1]);
             *reinterpret_cast<float2 *>(gred + w * 128 + (r + 8) * 8 + 2 * qq) = make_float2(d[2], d[3]);
         } else {
