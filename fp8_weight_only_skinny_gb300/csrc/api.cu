@@ -232,14 +232,20 @@ bool encode_weight_maps(PFN_cuTensorMapEncodeTiled_v12000 enc, bool nvfp4, const
     if (!enc3(tm_codes, codes, {32, row_bytes / 128, rows}, {128, row_bytes},
               {32, uint32_t(Traits<NVFP4>::SEGS), uint32_t(RG)}))
         return false;
-    // scales {word, row}: box [16 rows][64 B], 64-byte swizzle
+    // scales {word, row}: box [16 rows][64 B], 64-byte swizzle.  L2 promotion
+    // to 64 bytes, the box row itself: promoted to 256 bytes, each row fetch
+    // also brought in the next three chunks' scales, which the weight stream
+    // (evict-first) pushed out of L2 before the units that need them ran, so
+    // scale bytes came from DRAM up to four times (ncu on the lm_head at M = 8:
+    // DRAM reads 1.145 x the weight bytes; measured with 64-byte promotion:
+    // the lm_head 12 % faster, the decode stacks 1.4-1.8 %).
     const uint64_t srow = uint64_t(K) / 16;
     const cuuint64_t dims[2] = {srow / 4, rows};
     const cuuint64_t strides[1] = {srow};
     const cuuint32_t box[2] = {uint32_t(Traits<NVFP4>::SCALE_BOX_X), uint32_t(RG)};
     const cuuint32_t estr[2] = {1, 1};
     return enc(tm_scales, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(scales), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_64B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
