@@ -683,12 +683,36 @@ def run_ours(args):
 def run_profile_case(args):
     """A small, bounded workload for ncu: one layer shape at --m over --copies
     weight copies (each launch reads a different copy, so L2 is cold when the
-    copies total more than L2), run twice.  Launch order: copies x 2."""
+    copies total more than L2), run twice.  Launch order: copies x 2.
+
+    "stack:S" instead runs a shortened decode stack -- S layer sets (qkv,
+    o_proj FP8; gate_up, down NVFP4) and the lm_head -- three times in the
+    stack's order, eagerly with programmatic dependent launch: the DRAM
+    traffic of each kernel inside a stack whose weights L2 cannot hold."""
     import torch
 
     import fp8_weight_only_skinny_gb300 as sk
 
     name, fmt = args.profile.split(":")
+    if name == "stack":
+        torch.cuda.set_device(0)
+        dev = torch.device("cuda", 0)
+        sk.init()
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(5)
+        calls = [Linear(n, f, K, N, args.m, gen, dev) for _ in range(int(fmt)) for n, f, K, N in LAYER]
+        calls.append(LMHead(args.m, gen, dev))
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                for c in calls:
+                    c.call(sk)
+        s.synchronize()
+        st = sk.last_device_error()
+        if st != 0:
+            raise RuntimeError(f"device error {st}")
+        print(f"profile case stack of {fmt} layer sets + lm_head, M={args.m}: {len(calls)} calls x 3: ok")
+        return
     shapes = {n: (K, N) for n, _, K, N in [*LAYER, LM_HEAD]}
     K, N = shapes[name]
     torch.cuda.set_device(0)
@@ -757,7 +781,8 @@ def main():
                     help="only print the per-layer cold-L2 table (development A/B runs)")
     ap.add_argument("--profile", metavar="LAYER:FMT",
                     help="small profiling case: run one layer (e.g. gate_up:nvfp4, lm_head:nvfp4) "
-                         "over --copies distinct weight copies, twice, and exit")
+                         "over --copies distinct weight copies, twice, and exit; stack:S runs S layer "
+                         "sets and the lm_head three times")
     ap.add_argument("--copies", type=int, default=4)
     args = ap.parse_args()
     if args.profile:
