@@ -713,6 +713,24 @@ def run_profile_case(args):
             raise RuntimeError(f"device error {st}")
         print(f"profile case stack of {fmt} layer sets + lm_head, M={args.m}: {len(calls)} calls x 3: ok")
         return
+    if name == "quant":
+        # One FP16 weight of the gate_up shape (356 MB), quantized three times.
+        K, N = 5120, 34816
+        torch.cuda.set_device(0)
+        dev = torch.device("cuda", 0)
+        sk.init()
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(99)
+        w = (torch.randn((N, K), generator=gen, device=dev) * 0.02).to(torch.float16)
+        fn = {"fp8": sk.fp8_quantize, "nvfp4": sk.nvfp4_quantize}[fmt]
+        for _ in range(3):
+            fn(w)
+        torch.cuda.synchronize()
+        st = sk.last_device_error()
+        if st != 0:
+            raise RuntimeError(f"device error {st}")
+        print(f"profile case quant:{fmt} K={K} N={N} x 3: ok")
+        return
     shapes = {n: (K, N) for n, _, K, N in [*LAYER, LM_HEAD]}
     K, N = shapes[name]
     torch.cuda.set_device(0)
@@ -782,7 +800,8 @@ def main():
     ap.add_argument("--profile", metavar="LAYER:FMT",
                     help="small profiling case: run one layer (e.g. gate_up:nvfp4, lm_head:nvfp4) "
                          "over --copies distinct weight copies, twice, and exit; stack:S runs S layer "
-                         "sets and the lm_head three times")
+                         "sets and the lm_head three times; quant:FMT quantizes one FP16 gate_up "
+                         "weight three times")
     ap.add_argument("--copies", type=int, default=4)
     args = ap.parse_args()
     if args.profile:

@@ -8,8 +8,10 @@
 // order include/skinny.h states, so the result is bit-for-bit reproducible:
 // divisions and products use __fdiv_rn / __fmul_rn (no contraction), and the
 // final roundings use the hardware's nearest-even, saturating conversions
-// cvt.rn.satfinite.{e4m3x2,e2m1x2}.f32.  Both kernels are memory-bound
-// streams (read 2 bytes, write 1 or 0.5 byte per weight, 16-byte accesses).
+// cvt.rn.satfinite.{e4m3x2,e2m1x2}.f32.  The per-weight quotients are formed
+// by a product with the rounded reciprocal where that provably gives the same
+// code (quotient_codes).  Both kernels are memory-bound streams (read 2 bytes,
+// write 1 or 0.5 byte per weight, 16-byte accesses).
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -44,6 +46,43 @@ __device__ __forceinline__ float e4m3_value(uint32_t code) {
     return __half2float(__ushort_as_half(uint16_t(h2 & 0xFFFFu)));
 }
 
+// Codes of a quotient pair (x0 / d, x1 / d): each code is defined from the
+// binary32 quotient rounded to nearest-even, RN(x / d).  The kernels form
+// p = RN(x * r) with r = RN(1 / d), which is faster than the division and in
+// all but a few cases rounds to the same code.  The two roundings each add a
+// relative error of at most 2^-24, so |p - x / d| <= (2^-23 + 2^-48) |x / d|
+// and RN(x / d) lies within 3 units in the last place of x / d's binade from p,
+// always within 8 steps of p's bit pattern.  Rounding to a code, nearest with
+// saturation, is monotone in the magnitude: when the patterns 8 steps below and
+// above p (same sign) get p's code, every value between them gets it too,
+// RN(x / d) included, so p's code is taken; otherwise the pair is divided.  A
+// zero p fails the test (8 below it is a NaN pattern) and is divided as well.
+template <typename Cvt>
+__device__ __forceinline__ uint32_t quotient_codes(float x0, float x1, float d, float r, Cvt cvt) {
+    const float p0 = __fmul_rn(x0, r), p1 = __fmul_rn(x1, r);
+    const uint32_t c = cvt(p0, p1);
+    const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+    const uint32_t lo = cvt(__uint_as_float(b0 - 8u), __uint_as_float(b1 - 8u));
+    const uint32_t hi = cvt(__uint_as_float(b0 + 8u), __uint_as_float(b1 + 8u));
+    if (c == lo && c == hi) return c;
+    return cvt(__fdiv_rn(x0, d), __fdiv_rn(x1, d));
+}
+
+// Largest |value| of the eight FP16 values in v, as a bit pattern, folded into
+// m: with the sign cleared, FP16 bit patterns order like the magnitudes
+// (finite inputs).
+__device__ __forceinline__ uint32_t absmax_bits8(const uint4 &v, uint32_t m) {
+    m = __vmaxu2(m, v.x & 0x7FFF7FFFu);
+    m = __vmaxu2(m, v.y & 0x7FFF7FFFu);
+    m = __vmaxu2(m, v.z & 0x7FFF7FFFu);
+    return __vmaxu2(m, v.w & 0x7FFF7FFFu);
+}
+
+// The larger of the two FP16 bit patterns held in m2, as its FP32 value.
+__device__ __forceinline__ float half_bits_value(uint32_t m2) {
+    return __half2float(__ushort_as_half(uint16_t(__vmaxu2(m2, m2 >> 16) & 0xFFFFu)));
+}
+
 __device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -70,68 +109,65 @@ __device__ __forceinline__ float block_max(float a, float *red) {
     return red[0];
 }
 
-// FP8: persistent CTAs, each streaming 128 x 128 blocks (b = blockIdx.x,
-// blockIdx.x + gridDim.x, ...) through two shared-memory buffers filled by 2-D
-// TMA loads (rows or columns past N or K are zero-filled, which leaves the
-// block maximum unchanged).  Each thread keeps its 64 halves of the block in
-// registers: their absolute maximum, the block maximum (two barriers), then
-// the codes from the same registers.  The block's buffer is refilled with the
-// block two ahead as soon as every thread has read it, so each CTA keeps two
-// blocks in flight and HBM is read once per weight.
+// FP8: persistent CTAs, four per SM, each streaming 128 x 128 blocks
+// (b = blockIdx.x, blockIdx.x + gridDim.x, ...) through one shared-memory
+// buffer filled by 2-D TMA loads (rows or columns past N or K are zero-filled,
+// which leaves the block maximum unchanged).  Each thread keeps its 64 halves
+// of the block in registers: their absolute maximum (on the bit patterns), the
+// block maximum (two barriers), then the codes from the same registers.  The
+// buffer is refilled with the CTA's next block as soon as every thread has
+// read it, so that copy overlaps the codes of this one, and HBM is read once
+// per weight.  Measured on the gate_up shape against three CTAs per SM with
+// two buffers each: 112 -> 107 us; the CTAs' barriers, not the copies in
+// flight, set the pace (two CTAs of three buffers: 127 us; 512 threads: 118
+// us).
 constexpr int FQ_BLK = 128;
 constexpr int FQ_BUF = FQ_BLK * FQ_BLK * 2;          // 32 KB of FP16
-constexpr size_t FQ_SMEM = 1024 + 2 * FQ_BUF + 16;
+constexpr size_t FQ_SMEM = 1024 + FQ_BUF + 8;
+constexpr int FQ_CTAS_PER_SM = 4;                    // 64 registers x 256 threads x 4 fill the register file
 constexpr uint64_t FQ_WAIT_NS = 1000000000ull;       // bounded waits: ~1 s
 
-__global__ void __launch_bounds__(QT) fp8_quantize_kernel(const __grid_constant__ CUtensorMap tm_w, int N, int K,
+__global__ void __launch_bounds__(QT, FQ_CTAS_PER_SM) fp8_quantize_kernel(const __grid_constant__ CUtensorMap tm_w,
+                                                                          int N, int K,
                                                           int nbx, int nblocks, uint8_t *codes, float *scales) {
     extern __shared__ unsigned char fq_smem[];
     __shared__ float red[QT / 32];
     const uint32_t raw = sk::smem_u32(fq_smem);
     const uint32_t buf0 = (raw + 1023u) & ~1023u;
-    const uint32_t bar = buf0 + 2 * FQ_BUF;
+    const uint32_t bar = buf0 + FQ_BUF;
     const int tid = threadIdx.x;
     if (tid == 0) {
         sk::mbar_init(bar, 1);
-        sk::mbar_init(bar + 8, 1);
         sk::fence_barrier_init();
     }
     __syncthreads();
-    auto issue = [&](int blk, int b) {
-        sk::mbar_arrive_expect_tx(bar + 8 * b, FQ_BUF);
+    auto issue = [&](int blk) {
+        sk::mbar_arrive_expect_tx(bar, FQ_BUF);
         asm volatile(
             "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-            ::"r"(buf0 + b * FQ_BUF), "l"(reinterpret_cast<uint64_t>(&tm_w)), "r"((blk % nbx) * FQ_BLK),
-              "r"((blk / nbx) * FQ_BLK), "r"(bar + 8 * b)
+            ::"r"(buf0), "l"(reinterpret_cast<uint64_t>(&tm_w)), "r"((blk % nbx) * FQ_BLK),
+              "r"((blk / nbx) * FQ_BLK), "r"(bar)
             : "memory");
     };
-    if (tid == 0) {
-        if (int(blockIdx.x) < nblocks) issue(blockIdx.x, 0);
-        if (int(blockIdx.x + gridDim.x) < nblocks) issue(blockIdx.x + gridDim.x, 1);
-    }
+    if (tid == 0 && int(blockIdx.x) < nblocks) issue(blockIdx.x);
     int it = 0;
     for (int blk = blockIdx.x; blk < nblocks; blk += gridDim.x, ++it) {
-        const int b = it & 1;
         const uint64_t t0 = sk::globaltimer_ns();
-        while (!sk::mbar_try_wait(bar + 8 * b, (it >> 1) & 1)) {
+        while (!sk::mbar_try_wait(bar, it & 1)) {
             if (sk::globaltimer_ns() - t0 > FQ_WAIT_NS) return;   // copy never landed: give up (codes unspecified)
         }
         // Thread tid holds words tid + 256 i of the block: row tid / 16 + 16 i,
         // columns 8 (tid % 16) .. + 8 (a warp reads 512 contiguous bytes).
         uint4 v[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = sk::ld_shared_v4(buf0 + b * FQ_BUF + (tid + QT * i) * 16);
-        float a = 0.f;
+        for (int i = 0; i < 8; ++i) v[i] = sk::ld_shared_v4(buf0 + (tid + QT * i) * 16);
+        uint32_t m2 = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float f[8];
-            unpack8(v[i], f);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(f[j]));
-        }
-        a = block_max(a, red);          // its barriers also order every read of the buffer
-        if (tid == 0 && blk + 2 * int(gridDim.x) < nblocks) issue(blk + 2 * gridDim.x, b);
+        for (int i = 0; i < 8; ++i) m2 = absmax_bits8(v[i], m2);
+        const float a = block_max(half_bits_value(m2), red);   // its barriers also order every read of the buffer
+        if (tid == 0 && blk + int(gridDim.x) < nblocks) issue(blk + gridDim.x);
         const float s = a > 0.f ? __fdiv_rn(a, 448.f) : 1.f;
+        const float rs = __frcp_rn(s);
         const int r0 = (blk / nbx) * FQ_BLK, c0 = (blk % nbx) * FQ_BLK;
         if (tid == 0) scales[blk] = s;
 #pragma unroll
@@ -143,8 +179,8 @@ __global__ void __launch_bounds__(QT) fp8_quantize_kernel(const __grid_constant_
             uint32_t lo = 0, hi = 0;
 #pragma unroll
             for (int j = 0; j < 4; j += 2) {
-                lo |= e4m3x2_rn(__fdiv_rn(f[j], s), __fdiv_rn(f[j + 1], s)) << (8 * j);
-                hi |= e4m3x2_rn(__fdiv_rn(f[j + 4], s), __fdiv_rn(f[j + 5], s)) << (8 * j);
+                lo |= quotient_codes(f[j], f[j + 1], s, rs, e4m3x2_rn) << (8 * j);
+                hi |= quotient_codes(f[j + 4], f[j + 5], s, rs, e4m3x2_rn) << (8 * j);
             }
             *reinterpret_cast<uint2 *>(codes + size_t(r) * K + cc) = make_uint2(lo, hi);
         }
@@ -156,9 +192,24 @@ __global__ void __launch_bounds__(QT) fp8_quantize_kernel(const __grid_constant_
 __global__ void __launch_bounds__(QT) tensor_amax_kernel(const __half *w, long long n8, unsigned int *amax) {
     __shared__ float red[QT / 32];
     float a = 0.f;
-    for (long long i = blockIdx.x * (long long)QT + threadIdx.x; i < n8; i += (long long)gridDim.x * QT) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(w);
+    const long long stride = (long long)gridDim.x * QT;
+    long long i = blockIdx.x * (long long)QT + threadIdx.x;
+    for (; i + 3 * stride < n8; i += 4 * stride) {   // four independent loads in flight per thread
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = src[i + u * stride];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            float f[8];
+            unpack8(v[u], f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(f[j]));
+        }
+    }
+    for (; i < n8; i += stride) {
         float f[8];
-        unpack8(reinterpret_cast<const uint4 *>(w)[i], f);
+        unpack8(src[i], f);
 #pragma unroll
         for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(f[j]));
     }
@@ -174,8 +225,10 @@ __global__ void __launch_bounds__(QT) nvfp4_quantize_kernel(const __half *w, lon
     const float A = __uint_as_float(*amax);
     const float G = A > 0.f ? __fdiv_rn(A, 2688.f) : 1.f;
     if (blockIdx.x == 0 && threadIdx.x == 0) *gscale = G;
-    const long long b = blockIdx.x * (long long)QT + threadIdx.x;
-    if (b >= nblocks) return;
+    // Last block first: the maximum's pass ends on the tensor's tail, which is
+    // still in L2 when this pass starts.
+    const long long b = nblocks - 1 - (blockIdx.x * (long long)QT + threadIdx.x);
+    if (b < 0) return;
     float f[16];
     {
         const uint4 *src = reinterpret_cast<const uint4 *>(w + b * 16);
@@ -200,9 +253,10 @@ __global__ void __launch_bounds__(QT) nvfp4_quantize_kernel(const __half *w, lon
             if (__float_as_uint(f[i]) >> 31) out[i >> 3] |= 0x8u << (4 * (i & 7));
     } else {
         const float denom = __fmul_rn(S, G);
+        const float rd = __frcp_rn(denom);
 #pragma unroll
         for (int i = 0; i < 16; i += 2)
-            out[i >> 3] |= e2m1x2_rn(__fdiv_rn(f[i], denom), __fdiv_rn(f[i + 1], denom)) << (4 * (i & 7));
+            out[i >> 3] |= quotient_codes(f[i], f[i + 1], denom, rd, e2m1x2_rn) << (4 * (i & 7));
     }
     *reinterpret_cast<uint2 *>(codes + b * 8) = make_uint2(out[0], out[1]);
     scales[b] = uint8_t(sc);
@@ -235,7 +289,7 @@ sk_status fp8_quantize(const void *w, uint8_t *codes, float *scales, int N, int 
         attr_done[dev] = true;
     }
     const int sms = sk::device_sm_count();
-    const int cap = (sms > 0 ? sms : 1) * 3;                   // three CTAs (2 x 32 KB buffers) per SM
+    const int cap = (sms > 0 ? sms : 1) * FQ_CTAS_PER_SM;
     const int grid = nblocks < cap ? nblocks : cap;
     fp8_quantize_kernel<<<grid, QT, FQ_SMEM, reinterpret_cast<cudaStream_t>(stream)>>>(tm, N, K, int(nbx), nblocks,
                                                                                     codes, scales);
@@ -258,7 +312,8 @@ sk_status nvfp4_quantize(const void *w, uint8_t *codes, uint8_t *scales, float *
     if (cudaMemsetAsync(amax, 0, sizeof(unsigned int), s) != cudaSuccess) return SK_ERR_CUDA;
     if (n8 > 0) {
         const long long want = (n8 + QT - 1) / QT;
-        tensor_amax_kernel<<<int(want < 1024 ? want : 1024), QT, 0, s>>>(reinterpret_cast<const __half *>(w), n8,
+        const long long cap = 8LL * (sk::device_sm_count() > 0 ? sk::device_sm_count() : 1);
+        tensor_amax_kernel<<<int(want < cap ? want : cap), QT, 0, s>>>(reinterpret_cast<const __half *>(w), n8,
                                                                          amax);
     }
     const long long grid = nblocks > 0 ? (nblocks + QT - 1) / QT : 1;
