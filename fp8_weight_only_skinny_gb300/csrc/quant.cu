@@ -47,25 +47,26 @@ __device__ __forceinline__ float e4m3_value(uint32_t code) {
 }
 
 // Codes of a quotient pair (x0 / d, x1 / d): each code is defined from the
-// binary32 quotient rounded to nearest-even, RN(x / d).  The kernels form
+// binary32 quotient rounded to nearest-even, q = RN(x / d).  The kernels form
 // p = RN(x * r) with r = RN(1 / d), which is faster than the division and in
 // all but a few cases rounds to the same code.  The two roundings each add a
 // relative error of at most 2^-24, so |p - x / d| <= (2^-23 + 2^-48) |x / d|
-// and RN(x / d) lies within 3 units in the last place of x / d's binade from p,
-// always within 8 steps of p's bit pattern.  Rounding to a code, nearest with
-// saturation, is monotone in the magnitude: when the patterns 8 steps below and
-// above p (same sign) get p's code, every value between them gets it too,
-// RN(x / d) included, so p's code is taken; otherwise the pair is divided.  A
-// zero p fails the test (8 below it is a NaN pattern) and is divided as well.
-template <typename Cvt>
+// and q lies within 3 units in the last place of x / d's binade from p: within
+// 6 steps of p's bit pattern (3, or up to twice that where p and q sit in
+// neighbouring binades).  Every rounding boundary of the code format (a
+// midpoint between neighbouring values) has a binary32 pattern whose low bits
+// are zero: 19 bits for E4M3, subnormal midpoints included (MASK = 2^19 - 1),
+// 21 for E2M1 (MASK = 2^21 - 1).  Rounding to a code is monotone in the
+// magnitude, so p and q can get different codes only when a boundary lies
+// between them, hence within 6 steps of p; p's code is taken unless p's pattern
+// is within 8 steps of a multiple of MASK + 1, and the pair is divided then.
+// A zero p (x = 0) is such a multiple and is divided too.
+template <uint32_t MASK, typename Cvt>
 __device__ __forceinline__ uint32_t quotient_codes(float x0, float x1, float d, float r, Cvt cvt) {
     const float p0 = __fmul_rn(x0, r), p1 = __fmul_rn(x1, r);
-    const uint32_t c = cvt(p0, p1);
     const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
-    const uint32_t lo = cvt(__uint_as_float(b0 - 8u), __uint_as_float(b1 - 8u));
-    const uint32_t hi = cvt(__uint_as_float(b0 + 8u), __uint_as_float(b1 + 8u));
-    if (c == lo && c == hi) return c;
-    return cvt(__fdiv_rn(x0, d), __fdiv_rn(x1, d));
+    if (((b0 + 8u) & MASK) < 16u || ((b1 + 8u) & MASK) < 16u) return cvt(__fdiv_rn(x0, d), __fdiv_rn(x1, d));
+    return cvt(p0, p1);
 }
 
 // Largest |value| of the eight FP16 values in v, as a bit pattern, folded into
@@ -179,8 +180,8 @@ __global__ void __launch_bounds__(QT, FQ_CTAS_PER_SM) fp8_quantize_kernel(const 
             uint32_t lo = 0, hi = 0;
 #pragma unroll
             for (int j = 0; j < 4; j += 2) {
-                lo |= quotient_codes(f[j], f[j + 1], s, rs, e4m3x2_rn) << (8 * j);
-                hi |= quotient_codes(f[j + 4], f[j + 5], s, rs, e4m3x2_rn) << (8 * j);
+                lo |= quotient_codes<0x7FFFFu>(f[j], f[j + 1], s, rs, e4m3x2_rn) << (8 * j);
+                hi |= quotient_codes<0x7FFFFu>(f[j + 4], f[j + 5], s, rs, e4m3x2_rn) << (8 * j);
             }
             *reinterpret_cast<uint2 *>(codes + size_t(r) * K + cc) = make_uint2(lo, hi);
         }
@@ -256,7 +257,7 @@ __global__ void __launch_bounds__(QT) nvfp4_quantize_kernel(const __half *w, lon
         const float rd = __frcp_rn(denom);
 #pragma unroll
         for (int i = 0; i < 16; i += 2)
-            out[i >> 3] |= quotient_codes(f[i], f[i + 1], denom, rd, e2m1x2_rn) << (4 * (i & 7));
+            out[i >> 3] |= quotient_codes<0x1FFFFFu>(f[i], f[i + 1], denom, rd, e2m1x2_rn) << (4 * (i & 7));
     }
     *reinterpret_cast<uint2 *>(codes + b * 8) = make_uint2(out[0], out[1]);
     scales[b] = uint8_t(sc);
