@@ -246,11 +246,11 @@ def capture(fn, stream):
 
 
 def layer_table(sk, gen, dev, stream, peak, tp=False):
-    """Per-layer cold-L2 rates at M = 1 and 8, both formats (the lm_head in
-    NVFP4), at the full shapes or at the per-rank shapes of 4-way tensor
-    parallelism."""
+    """Per-layer cold-L2 rates, both formats (the lm_head in NVFP4): at the full
+    shapes for M = 1, 2, 4 and 8, at the per-rank shapes of 4-way tensor
+    parallelism for M = 1 and 8."""
     rows = []
-    for mm in (1, 8):
+    for mm in ((1, 8) if tp else (1, 2, 4, 8)):
         for name, f, K, N in LAYER + [LM_HEAD]:
             Ks, Ns = tp_shape(name, K, N) if tp else (K, N)
             for fmt in ((f,) if name == "lm_head" else ("nvfp4", "fp8")):
