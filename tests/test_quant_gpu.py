@@ -144,6 +144,58 @@ def test_exact_ties_round_to_even(sk):
     assert np.array_equal(host(codes), c_ref) and np.array_equal(host(scales), s_ref)
 
 
+def test_nvfp4_quotients_on_the_boundary_grid(sk):
+    """Weights whose quotients w / (S G) are exactly E2M1 values or midpoints
+    between them (G = 2^-10, every 16-block's scale an exact E4M3 value S): the
+    kernel's products land on or next to its boundary grid almost everywhere,
+    so nearly every pair takes the division path -- bitwise against the oracle."""
+    r = np.random.default_rng(71)
+    N, K = 256, 1024
+    G = 2.0 ** -10
+    vals = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5])
+    S = oracle.e4m3_to_f64(np.arange(0x08, 0x60))[r.integers(0, 0x58, (N, K // 16))]
+    m = r.choice(vals, (N, K // 16, 16)) * r.choice([-1.0, 1.0], (N, K // 16, 16))
+    m[:, :, 0] = 6.0                                   # each block's maximum: 6 S G, so its scale is S
+    w64 = (m * (S * G)[:, :, None]).reshape(N, K)
+    w64[0, :16] = 0.0
+    w64[0, 0] = 2688 * G                               # the tensor maximum: G = 2^-10
+    w = w64.astype(F16)
+    assert np.array_equal(w.astype(np.float64), w64)   # every weight exact in FP16
+    codes, scales, g = sk.nvfp4_quantize(dev(w))
+    c_ref, s_ref, g_ref = oracle.quantize_nvfp4(w)
+    assert g_ref == np.float32(G) and np.float32(host(g)[0]) == g_ref
+    assert np.array_equal(host(scales), s_ref)
+    got = host(codes)
+    assert np.array_equal(got, c_ref), int(np.sum(got != c_ref))
+
+
+def test_fp8_quotients_on_the_boundary_grid(sk):
+    """FP8 blocks whose scale s = max|w| / 448 is 2^-8 times 1, 1.25, 1.5 or 1.75
+    and whose weights are s times E4M3 values or midpoints between them (each
+    block holding +-448 s): w / s is exact, its product with RN(1/s) sits on or
+    next to the boundary grid, and the division path decides -- bitwise against
+    the oracle."""
+    r = np.random.default_rng(72)
+    N, K = 384, 512
+    e = oracle.e4m3_to_f64(np.arange(0x7F))
+    vals = np.concatenate([e, (e[:-1] + e[1:]) / 2])
+    vals = vals[(vals <= 448) & (vals >= 2.0 ** -9)]
+    w64 = np.zeros((N, K))
+    for i in range(N // 128):
+        for j in range(K // 128):
+            s = 2.0 ** -8 * r.choice([1.0, 1.25, 1.5, 1.75])
+            v = r.choice(vals, (128, 128)) * r.choice([-1.0, 1.0], (128, 128))
+            v[0, 0] = 448.0
+            w64[i * 128:(i + 1) * 128, j * 128:(j + 1) * 128] = v * s
+    w = w64.astype(F16)
+    assert np.array_equal(w.astype(np.float64), w64)   # every weight exact in FP16
+    codes, scales = sk.fp8_quantize(dev(w))
+    c_ref, s_ref = oracle.quantize_fp8(w)
+    assert np.array_equal(host(scales).astype(np.float32), s_ref)
+    got = host(codes)
+    assert np.array_equal(got, c_ref), int(np.sum(got != c_ref))
+
+
 @pytest.mark.parametrize("M", [1, 8])
 def test_quantized_weights_feed_the_linears(sk, M):
     """GPU-quantized weights through nvfp4_gemm / fp8_gemm meet the oracle
