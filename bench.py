@@ -713,6 +713,25 @@ def run_profile_case(args):
             raise RuntimeError(f"device error {st}")
         print(f"profile case stack of {fmt} layer sets + lm_head, M={args.m}: {len(calls)} calls x 3: ok")
         return
+    if name == "sample":
+        # The sampled lm_head (temperature 0.6, top-k 50, top-p 0.9) at --m rows,
+        # three calls: the projection kernel, then the cluster sampler.
+        torch.cuda.set_device(0)
+        dev = torch.device("cuda", 0)
+        sk.init()
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(99)
+        head = LMHead(args.m, gen, dev)
+        u = torch.rand((args.m,), generator=gen, device=dev)
+        tok = torch.empty((args.m,), dtype=torch.int32, device=dev)
+        for _ in range(3):
+            sk.lm_head_sample(head.x, head.codes, head.scales, head.g, u, 0.6, 50, 0.9, logits=head.y, token=tok)
+        torch.cuda.synchronize()
+        st = sk.last_device_error()
+        if st != 0:
+            raise RuntimeError(f"device error {st}")
+        print(f"profile case sample M={args.m} x 3: ok")
+        return
     if name == "quant":
         # One FP16 weight of the gate_up shape (356 MB), quantized three times.
         K, N = 5120, 34816
@@ -801,7 +820,7 @@ def main():
                     help="small profiling case: run one layer (e.g. gate_up:nvfp4, lm_head:nvfp4) "
                          "over --copies distinct weight copies, twice, and exit; stack:S runs S layer "
                          "sets and the lm_head three times; quant:FMT quantizes one FP16 gate_up "
-                         "weight three times")
+                         "weight three times; sample:lm_head runs the sampled lm_head three times")
     ap.add_argument("--copies", type=int, default=4)
     args = ap.parse_args()
     if args.profile:
