@@ -52,6 +52,20 @@ def test_lm_head_logits_and_argmax(sk, M, K, N):
     assert np.array_equal(am2, am)
 
 
+@pytest.mark.parametrize("M", [1, 8])
+@pytest.mark.parametrize("K", [17408, 32768])
+def test_lm_head_many_chunks(sk, M, K):
+    """17 and 32 k-chunks per row group: the argmax through the owners'
+    many-chunk sums (one and two rounds of 24 slots), ragged N."""
+    N = 1001
+    x = synth.x_f16(M, K, seed=K + M)
+    codes, scales, g = synth.nvfp4_weights(N, K, seed=K)
+    y_ref, l1 = oracle.nvfp4_linear(x, codes, scales, g)
+    lg, am = _guarded_head(sk, x, codes, scales, g, M, N)
+    check(lg, y_ref, l1, False, f"lm_head logits K={K}")
+    _argmax_ok(am, y_ref, l1, lg)
+
+
 def test_ties_go_to_the_lowest_index(sk):
     M, K, N = 8, 1024, 700
     x = synth.x_f16(M, K, seed=5)

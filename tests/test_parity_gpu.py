@@ -126,6 +126,23 @@ def test_long_k_many_partials(sk, M, var):
         check(f8_run(sk, x, c8, s8), f_ref, fl1, False, "fp8 long K")
 
 
+@pytest.mark.parametrize("M,var", ONE_AND_EIGHT)
+@pytest.mark.parametrize("K", [32768, 49408])
+def test_very_long_k_several_fixup_rounds(sk, K, M, var):
+    """32 and 49 k-chunks per row group (the last one ragged at K = 49408):
+    the owners sum the partial slots of a row group in rounds of 24 chunks, so
+    these take two and three rounds; N = 77 leaves a ragged row group."""
+    N = 77
+    x = synth.x_f16(M, K, seed=23)
+    codes, scales, g = synth.nvfp4_weights(N, K, seed=23)
+    y_ref, l1 = oracle.nvfp4_linear(x, codes, scales, g)
+    c8, s8 = synth.fp8_weights(N, K, seed=24)
+    f_ref, fl1 = oracle.fp8_linear(x, c8, s8)
+    with variant(sk, var):
+        check(nv_run(sk, x, codes, scales, g), y_ref, l1, False, f"nvfp4 K={K}")
+        check(f8_run(sk, x, c8, s8), f_ref, fl1, False, f"fp8 K={K}")
+
+
 # ------------------------------------------------- exact / bitwise cases ---
 
 @pytest.mark.parametrize("M,var", ONE_AND_EIGHT)
