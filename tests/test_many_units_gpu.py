@@ -37,7 +37,9 @@ MV = [(1, "simt"), (1, "tensor"), (2, "auto"), (4, "auto"), (8, "auto")]
 
 
 @pytest.mark.parametrize("M,var", MV)
-@pytest.mark.parametrize("K,N", [(1024, 520), (3072, 200), (5120, 96)])
+# K = 10240: ten k-chunks, the owners' many-chunk sums, each owner summing
+# several row groups in turn on the capped grids.
+@pytest.mark.parametrize("K,N", [(1024, 520), (3072, 200), (5120, 96), (10240, 520)])
 def test_nvfp4_many_units_per_cta(sk, max_ctas, M, var, K, N):
     x = synth.x_f16(M, K, seed=K + M)
     codes, scales, g = synth.nvfp4_weights(N, K, seed=N + 1)
@@ -51,7 +53,7 @@ def test_nvfp4_many_units_per_cta(sk, max_ctas, M, var, K, N):
 
 
 @pytest.mark.parametrize("M,var", MV)
-@pytest.mark.parametrize("K,N", [(1024, 520), (3072, 200), (4096, 130)])
+@pytest.mark.parametrize("K,N", [(1024, 520), (3072, 200), (4096, 130), (10240, 264)])
 def test_fp8_many_units_per_cta(sk, max_ctas, M, var, K, N):
     x = synth.x_f16(M, K, seed=K + M + 5)
     codes, scales = synth.fp8_weights(N, K, seed=N + 2)
