@@ -221,24 +221,16 @@ __global__ void __launch_bounds__(QT) tensor_amax_kernel(const __half *w, long l
 
 // One thread per 16-element block of a row (row-major, so block b starts at
 // element 16 b): its E4M3 scale and its eight code bytes.
-__global__ void __launch_bounds__(QT) nvfp4_quantize_kernel(const __half *w, long long nblocks,
-                                                            const unsigned int *amax, uint8_t *codes,
-                                                            uint8_t *scales, float *gscale) {
-    const float A = __uint_as_float(*amax);
-    const float G = A > 0.f ? __fdiv_rn(A, 2688.f) : 1.f;
-    if (blockIdx.x == 0 && threadIdx.x == 0) *gscale = G;
-    // Last block first: the maximum's pass ends on the tensor's tail, which is
-    // still in L2 when this pass starts.
-    const long long b = nblocks - 1 - (blockIdx.x * (long long)QT + threadIdx.x);
-    if (b < 0) return;
+// One 16-weight block (two 16-byte words of FP16): its E4M3 scale code and
+// its eight code bytes.
+__device__ __forceinline__ uint32_t encode_block(const uint4 &v0, const uint4 &v1, float G, uint2 &cw) {
     float f[16];
     {
-        const uint4 *src = reinterpret_cast<const uint4 *>(w + b * 16);
         float t[8];
-        unpack8(src[0], t);
+        unpack8(v0, t);
 #pragma unroll
         for (int i = 0; i < 8; ++i) f[i] = t[i];
-        unpack8(src[1], t);
+        unpack8(v1, t);
 #pragma unroll
         for (int i = 0; i < 8; ++i) f[8 + i] = t[i];
     }
@@ -260,8 +252,48 @@ __global__ void __launch_bounds__(QT) nvfp4_quantize_kernel(const __half *w, lon
         for (int i = 0; i < 16; i += 2)
             out[i >> 3] |= quotient_codes<0x1FFFFFu>(f[i], f[i + 1], denom, rd, e2m1x2_rn) << (4 * (i & 7));
     }
-    *reinterpret_cast<uint2 *>(codes + b * 8) = make_uint2(out[0], out[1]);
-    scales[b] = uint8_t(sc);
+    cw = make_uint2(out[0], out[1]);
+    return sc;
+}
+
+// One thread per two consecutive 16-element blocks of a row-major tensor
+// (blocks 2j and 2j + 1 start at elements 32 j and 32 j + 16): two blocks'
+// loads and arithmetic in flight per thread.  Measured on the gate_up shape
+// against one block per thread: 145 -> 139 us (152 -> 147 us on a weight draw
+// with more products near the boundary grid); four per thread: 170 us.
+__global__ void __launch_bounds__(QT) nvfp4_quantize_kernel(const __half *w, long long nblocks,
+                                                            const unsigned int *amax, uint8_t *codes,
+                                                            uint8_t *scales, float *gscale) {
+    const float A = __uint_as_float(*amax);
+    const float G = A > 0.f ? __fdiv_rn(A, 2688.f) : 1.f;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *gscale = G;
+    // Last pair first: the maximum's pass ends on the tensor's tail, which is
+    // still in L2 when this pass starts.
+    const long long npairs = (nblocks + 1) / 2;
+    const long long pr = npairs - 1 - (blockIdx.x * (long long)QT + threadIdx.x);
+    if (pr < 0) return;
+    const long long b = 2 * pr;
+    const bool two = b + 1 < nblocks;
+    const uint4 *src = reinterpret_cast<const uint4 *>(w + b * 16);
+    const uint4 v0 = src[0], v1 = src[1];
+    uint4 v2 = make_uint4(0, 0, 0, 0), v3 = v2;
+    if (two) {
+        v2 = src[2];
+        v3 = src[3];
+    }
+    uint2 c0, c1;
+    const uint32_t s0 = encode_block(v0, v1, G, c0);
+    if (two) {
+        const uint32_t s1 = encode_block(v2, v3, G, c1);
+        // codes and scales are only 8-byte and 1-byte aligned: 8-byte and byte stores
+        *reinterpret_cast<uint2 *>(codes + b * 8) = c0;
+        *reinterpret_cast<uint2 *>(codes + b * 8 + 8) = c1;
+        scales[b] = uint8_t(s0);
+        scales[b + 1] = uint8_t(s1);
+    } else {
+        *reinterpret_cast<uint2 *>(codes + b * 8) = c0;
+        scales[b] = uint8_t(s0);
+    }
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -318,7 +350,8 @@ sk_status nvfp4_quantize(const void *w, uint8_t *codes, uint8_t *scales, float *
         tensor_amax_kernel<<<int(want < cap ? want : cap), QT, 0, s>>>(reinterpret_cast<const __half *>(w), n8,
                                                                          amax);
     }
-    const long long grid = nblocks > 0 ? (nblocks + QT - 1) / QT : 1;
+    const long long pairs = (nblocks + 1) / 2;
+    const long long grid = pairs > 0 ? (pairs + QT - 1) / QT : 1;
     if (grid > 0x7FFFFFFFLL) return SK_ERR_UNSUPPORTED_SHAPE;
     nvfp4_quantize_kernel<<<unsigned(grid), QT, 0, s>>>(reinterpret_cast<const __half *>(w), nblocks, amax, codes,
                                                         scales, gscale);
