@@ -3,12 +3,13 @@
 // the pages describe samples at a temperature (page "NVFP4 在 Volta 上！", the
 // "温度 0.6" run) besides the greedy pick; include/skinny.h states the rule.
 //
-// One thread-block cluster of SC CTAs per row, each CTA holding a contiguous
-// slice of the row (copied into shared memory with every copy in flight at
-// once): (1) a radix select, 8 bits at a time, finds the top_k-th largest of
-// the row's ordered FP32 keys -- each CTA counts its slice into a histogram,
-// and every CTA sums all SC histograms through distributed shared memory (two
-// remote reads per thread) to take the same decision; (2) every CTA writes its
+// One thread-block cluster of SC CTAs per row (16 for up to four rows, else
+// 8), each CTA holding a contiguous slice of the row (copied into shared
+// memory with every copy in flight at once): (1) a radix select, 8 bits at a
+// time, finds the top_k-th largest of the row's ordered FP32 keys -- each CTA
+// counts its slice into a histogram, and every CTA sums all SC histograms
+// through distributed shared memory (SC / 4 remote reads per thread) to take
+// the same decision; (2) every CTA writes its
 // candidates (keys above that threshold, then keys equal to it, lowest index
 // first) straight into the first CTA's shared memory, at offsets from the
 // CTAs' published counts, each thread scanning one contiguous run of keys.
@@ -94,8 +95,12 @@ __device__ __forceinline__ float block_scan(float v, float *warp_sum) {
     return r;
 }
 
-constexpr int SC = 8;          // CTAs per row: one portable-size cluster
-constexpr int CACHE = 49152;   // keys of a slice kept in shared memory (192 KB); the rest re-read from L2
+constexpr int CACHE = 49152;
+// Rows per call up to which each row gets a 16-CTA cluster: measured on the
+// 151936-wide vocabulary, 16 CTAs per row were 3.4-3.9 us faster per call at
+// M = 1, 2 and 4 (half the slice per CTA to count and scan) and 5.4 us slower
+// at M = 8 (eight 16-CTA clusters no longer each get SMs of their own).
+constexpr int WIDE_MAX_M = 4;   // keys of a slice kept in shared memory (192 KB); the rest re-read from L2
 
 __device__ __forceinline__ unsigned int cluster_rank() {
     unsigned int r;
@@ -144,10 +149,12 @@ __device__ __forceinline__ unsigned long long cand_key(unsigned int key, int ind
     return (static_cast<unsigned long long>(key) << 32) | static_cast<unsigned int>(~index);
 }
 
-static_assert(ST == 4 * 256 && SC == 8, "the histogram merge gives each thread two of the eight ranks");
 
+// SC CTAs per row, one cluster: 8 (portable) or 16 (a non-portable size).
+template <int SC>
 __global__ void __cluster_dims__(SC, 1, 1) __launch_bounds__(ST)
     sample_kernel(const float *logits, int N, const float *u, float T, int top_k, float top_p, int32_t *token) {
+    static_assert(ST == 4 * 256 && SC % 4 == 0, "the histogram merge gives each thread SC / 4 of the ranks");
     extern __shared__ unsigned int skey[];           // this slice's FP32 bits (up to CACHE)
     __shared__ unsigned int hist[2][256];            // per pass, double-buffered across the cluster
     __shared__ unsigned int part[4][256];            // cluster totals of one pass, two ranks per row
@@ -202,10 +209,15 @@ __global__ void __cluster_dims__(SC, 1, 1) __launch_bounds__(ST)
         }
         cluster_sync();
         {
-            // every thread reads one bin of two ranks (both loads in flight together)
+            // every thread reads one bin of SC / 4 ranks (all loads in flight together)
             const unsigned int b = unsigned(tid) & 255u, r0 = unsigned(tid) >> 8;
-            const unsigned int v0 = ld_dsmem(dsmem_addr(h + b, r0)), v1 = ld_dsmem(dsmem_addr(h + b, r0 + 4));
-            part[r0][b] = v0 + v1;
+            unsigned int v[SC / 4];
+#pragma unroll
+            for (int j = 0; j < SC / 4; ++j) v[j] = ld_dsmem(dsmem_addr(h + b, r0 + 4u * unsigned(j)));
+            unsigned int t = 0u;
+#pragma unroll
+            for (int j = 0; j < SC / 4; ++j) t += v[j];
+            part[r0][b] = t;
         }
         __syncthreads();
         // Thread t < 256 takes bin 255 - t: an inclusive scan over t is the
@@ -400,12 +412,25 @@ sk_status lm_head_sample(const void *x, const uint8_t *W_codes, const uint8_t *W
     if (!aligned4(u) || !aligned4(token)) return SK_ERR_MISALIGNED;
     const sk_status st = nvfp4_gemm(x, W_codes, W_scales, W_gscale, logits, M, N, K, stream);
     if (st != SK_OK) return st;
-    const int slice = (N + SC - 1) / SC;
+    // Few rows: 16 CTAs per row (half the slice per CTA); more rows: 8, so that
+    // every row's cluster fits beside the others.
+    const bool wide = M <= WIDE_MAX_M;
+    const int SCn = wide ? 16 : 8;
+    const int slice = (N + SCn - 1) / SCn;
     const size_t smem = size_t(slice < CACHE ? slice : CACHE) * sizeof(unsigned int);
-    if (cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
-        return SK_ERR_CUDA;
-    sample_kernel<<<M * SC, ST, smem, reinterpret_cast<cudaStream_t>(stream)>>>(logits, N, u, temperature, top_k,
-                                                                              top_p, token);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (wide) {
+        if (cudaFuncSetAttribute(sample_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(sample_kernel<16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+            return SK_ERR_CUDA;
+        sample_kernel<16><<<M * 16, ST, smem, s>>>(logits, N, u, temperature, top_k, top_p, token);
+    } else {
+        if (cudaFuncSetAttribute(sample_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+            cudaSuccess)
+            return SK_ERR_CUDA;
+        sample_kernel<8><<<M * 8, ST, smem, s>>>(logits, N, u, temperature, top_k, top_p, token);
+    }
     return cudaGetLastError() == cudaSuccess ? SK_OK : SK_ERR_CUDA;
 }
 
