@@ -3,8 +3,8 @@
 // the pages describe samples at a temperature (page "NVFP4 在 Volta 上！", the
 // "温度 0.6" run) besides the greedy pick; include/skinny.h states the rule.
 //
-// One thread-block cluster of SC CTAs per row (16 for up to four rows, else
-// 8), each CTA holding a contiguous slice of the row (copied into shared
+// One thread-block cluster of SC CTAs per row (16 for up to seven rows, 8 for
+// eight), each CTA holding a contiguous slice of the row (copied into shared
 // memory with every copy in flight at once): (1) a radix select, 8 bits at a
 // time, finds the top_k-th largest of the row's ordered FP32 keys -- each CTA
 // counts its slice into a histogram, and every CTA sums all SC histograms
@@ -98,9 +98,9 @@ __device__ __forceinline__ float block_scan(float v, float *warp_sum) {
 constexpr int CACHE = 49152;
 // Rows per call up to which each row gets a 16-CTA cluster: measured on the
 // 151936-wide vocabulary, 16 CTAs per row were 3.4-3.9 us faster per call at
-// M = 1, 2 and 4 (half the slice per CTA to count and scan) and 5.4 us slower
-// at M = 8 (eight 16-CTA clusters no longer each get SMs of their own).
-constexpr int WIDE_MAX_M = 4;   // keys of a slice kept in shared memory (192 KB); the rest re-read from L2
+// M = 1 to 7 (half the slice per CTA to count and scan) and 4-5.4 us slower at
+// M = 8, also with one CTA per SM forced.
+constexpr int WIDE_MAX_M = 7;   // keys of a slice kept in shared memory (192 KB); the rest re-read from L2
 
 __device__ __forceinline__ unsigned int cluster_rank() {
     unsigned int r;
@@ -412,8 +412,7 @@ sk_status lm_head_sample(const void *x, const uint8_t *W_codes, const uint8_t *W
     if (!aligned4(u) || !aligned4(token)) return SK_ERR_MISALIGNED;
     const sk_status st = nvfp4_gemm(x, W_codes, W_scales, W_gscale, logits, M, N, K, stream);
     if (st != SK_OK) return st;
-    // Few rows: 16 CTAs per row (half the slice per CTA); more rows: 8, so that
-    // every row's cluster fits beside the others.
+    // Up to seven rows: 16 CTAs per row (half the slice per CTA); eight: 8.
     const bool wide = M <= WIDE_MAX_M;
     const int SCn = wide ? 16 : 8;
     const int slice = (N + SCn - 1) / SCn;
