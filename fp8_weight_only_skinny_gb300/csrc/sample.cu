@@ -3,7 +3,7 @@
 // the pages describe samples at a temperature (page "NVFP4 在 Volta 上！", the
 // "温度 0.6" run) besides the greedy pick; include/skinny.h states the rule.
 //
-// One thread-block cluster of SC CTAs per row (16 for up to seven rows, 8 for
+// One thread-block cluster of SC CTAs per row (16 for up to seven rows, 12 for
 // eight), each CTA holding a contiguous slice of the row (copied into shared
 // memory with every copy in flight at once): (1) a radix select, 8 bits at a
 // time, finds the top_k-th largest of the row's ordered FP32 keys -- each CTA
@@ -96,10 +96,11 @@ __device__ __forceinline__ float block_scan(float v, float *warp_sum) {
 }
 
 constexpr int CACHE = 49152;
-// Rows per call up to which each row gets a 16-CTA cluster: measured on the
-// 151936-wide vocabulary, 16 CTAs per row were 3.4-3.9 us faster per call at
-// M = 1 to 7 (half the slice per CTA to count and scan) and 4-5.4 us slower at
-// M = 8, also with one CTA per SM forced.
+// CTAs per row (non-portable cluster sizes): 16 for up to WIDE_MAX_M rows, 12
+// for more.  Measured on the 151936-wide vocabulary against 8 CTAs per row:
+// 16 were 3.4-3.9 us faster per call at M = 1 to 7 (half the slice per CTA to
+// count and scan) but 4-5.4 us slower at M = 8, also with one CTA per SM
+// forced; 12 were 2.2-2.9 us faster at M = 8.
 constexpr int WIDE_MAX_M = 7;   // keys of a slice kept in shared memory (192 KB); the rest re-read from L2
 
 __device__ __forceinline__ unsigned int cluster_rank() {
@@ -150,7 +151,7 @@ __device__ __forceinline__ unsigned long long cand_key(unsigned int key, int ind
 }
 
 
-// SC CTAs per row, one cluster: 8 (portable) or 16 (a non-portable size).
+// SC CTAs per row, one cluster (a multiple of 4; 12 and 16 are non-portable sizes).
 template <int SC>
 __global__ void __cluster_dims__(SC, 1, 1) __launch_bounds__(ST)
     sample_kernel(const float *logits, int N, const float *u, float T, int top_k, float top_p, int32_t *token) {
@@ -397,6 +398,19 @@ __global__ void __cluster_dims__(SC, 1, 1) __launch_bounds__(ST)
 
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
+template <int SC>
+sk_status launch_sample(const float *logits, int N, const float *u, float T, int top_k, float top_p,
+                        int32_t *token, int M, cudaStream_t s) {
+    const int slice = (N + SC - 1) / SC;
+    const size_t smem = size_t(slice < CACHE ? slice : CACHE) * sizeof(unsigned int);
+    if (cudaFuncSetAttribute(sample_kernel<SC>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(sample_kernel<SC>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        return SK_ERR_CUDA;
+    sample_kernel<SC><<<M * SC, ST, smem, s>>>(logits, N, u, T, top_k, top_p, token);
+    return cudaGetLastError() == cudaSuccess ? SK_OK : SK_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -412,25 +426,9 @@ sk_status lm_head_sample(const void *x, const uint8_t *W_codes, const uint8_t *W
     if (!aligned4(u) || !aligned4(token)) return SK_ERR_MISALIGNED;
     const sk_status st = nvfp4_gemm(x, W_codes, W_scales, W_gscale, logits, M, N, K, stream);
     if (st != SK_OK) return st;
-    // Up to seven rows: 16 CTAs per row (half the slice per CTA); eight: 8.
-    const bool wide = M <= WIDE_MAX_M;
-    const int SCn = wide ? 16 : 8;
-    const int slice = (N + SCn - 1) / SCn;
-    const size_t smem = size_t(slice < CACHE ? slice : CACHE) * sizeof(unsigned int);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (wide) {
-        if (cudaFuncSetAttribute(sample_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
-                cudaSuccess ||
-            cudaFuncSetAttribute(sample_kernel<16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-            return SK_ERR_CUDA;
-        sample_kernel<16><<<M * 16, ST, smem, s>>>(logits, N, u, temperature, top_k, top_p, token);
-    } else {
-        if (cudaFuncSetAttribute(sample_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
-            cudaSuccess)
-            return SK_ERR_CUDA;
-        sample_kernel<8><<<M * 8, ST, smem, s>>>(logits, N, u, temperature, top_k, top_p, token);
-    }
-    return cudaGetLastError() == cudaSuccess ? SK_OK : SK_ERR_CUDA;
+    return M <= WIDE_MAX_M ? launch_sample<16>(logits, N, u, temperature, top_k, top_p, token, M, s)
+                           : launch_sample<12>(logits, N, u, temperature, top_k, top_p, token, M, s);
 }
 
 }  // extern "C"
