@@ -95,13 +95,13 @@ __device__ __forceinline__ float block_scan(float v, float *warp_sum) {
     return r;
 }
 
-constexpr int CACHE = 49152;
+constexpr int CACHE = 49152;   // keys of a slice kept in shared memory (192 KB); the rest re-read from L2
 // CTAs per row (non-portable cluster sizes): 16 for up to WIDE_MAX_M rows, 12
 // for more.  Measured on the 151936-wide vocabulary against 8 CTAs per row:
 // 16 were 3.4-3.9 us faster per call at M = 1 to 7 (half the slice per CTA to
 // count and scan) but 4-5.4 us slower at M = 8, also with one CTA per SM
 // forced; 12 were 2.2-2.9 us faster at M = 8.
-constexpr int WIDE_MAX_M = 7;   // keys of a slice kept in shared memory (192 KB); the rest re-read from L2
+constexpr int WIDE_MAX_M = 7;
 
 __device__ __forceinline__ unsigned int cluster_rank() {
     unsigned int r;
@@ -150,7 +150,6 @@ __device__ __forceinline__ unsigned long long cand_key(unsigned int key, int ind
     return (static_cast<unsigned long long>(key) << 32) | static_cast<unsigned int>(~index);
 }
 
-
 // SC CTAs per row, one cluster (a multiple of 4; 12 and 16 are non-portable sizes).
 template <int SC>
 __global__ void __cluster_dims__(SC, 1, 1) __launch_bounds__(ST)
@@ -158,7 +157,7 @@ __global__ void __cluster_dims__(SC, 1, 1) __launch_bounds__(ST)
     static_assert(ST == 4 * 256 && SC % 4 == 0, "the histogram merge gives each thread SC / 4 of the ranks");
     extern __shared__ unsigned int skey[];           // this slice's FP32 bits (up to CACHE)
     __shared__ unsigned int hist[2][256];            // per pass, double-buffered across the cluster
-    __shared__ unsigned int part[4][256];            // cluster totals of one pass, two ranks per row
+    __shared__ unsigned int part[4][256];            // cluster totals of one pass, SC / 4 ranks per row
     __shared__ unsigned long long cand[ST];          // used in the first CTA of the cluster
     __shared__ float cum[ST];
     __shared__ unsigned long long warp_u64[8];
