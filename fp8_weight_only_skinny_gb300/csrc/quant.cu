@@ -219,8 +219,6 @@ __global__ void __launch_bounds__(QT) tensor_amax_kernel(const __half *w, long l
     if (threadIdx.x == 0) atomicMax(amax, __float_as_uint(a));
 }
 
-// One thread per 16-element block of a row (row-major, so block b starts at
-// element 16 b): its E4M3 scale and its eight code bytes.
 // One 16-weight block (two 16-byte words of FP16): its E4M3 scale code and
 // its eight code bytes.
 __device__ __forceinline__ uint32_t encode_block(const uint4 &v0, const uint4 &v1, float G, uint2 &cw) {
