@@ -311,6 +311,8 @@ int choose_mp(int M, bool nvfp4, long long U, long long P) {
     return per_cta >= (nvfp4 ? 96 : 24) ? 1 : 8;
 }
 
+bool pdl_enabled() { return g_pdl != 0; }
+
 }  // namespace sk
 
 extern "C" {

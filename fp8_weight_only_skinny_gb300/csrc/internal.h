@@ -68,6 +68,9 @@ unsigned char *workspace_for(cudaStream_t stream);
 // = 1.  The values loaded, and so the results, do not change.
 bool use_wide_x(const void *x, int M);
 
+// Whether launches may use programmatic dependent launch (sk_set_pdl).
+bool pdl_enabled();
+
 // Token slots of the kernel variant for an M-token call of U units on a grid
 // of P CTAs: 1 (SIMT) or 8 (tensor-core), by the process-wide variant setting.
 int choose_mp(int M, bool nvfp4, long long U, long long P);
